@@ -1,0 +1,198 @@
+// Lightning Indexer oracle: plain, slow fp64 CPU restatement of the scoring rule and the
+// Top-512 selection. TEST INFRASTRUCTURE ONLY: tests, the smoke check and the benchmark's CPU
+// baseline call it; the product library never links or loads it, and it shares no code with
+// the CUDA path.
+//
+// What it follows:
+//  * "DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화" (aitrends), sections 섹션별 상세 and
+//    용어 해설 (Lightning Indexer, Sparse Attention): the indexer scores the positions a query
+//    can attend to and a Top-512 selection keeps the best ones for sparse attention. The page
+//    prints no formula; the rule restated here is the DeepSeek sparse-attention indexer score
+//        I[t,s] = kscale[s] * sum_j w[t,j] * max(0, sum_i q[t,j,i] * k[s,i])
+//    over the index heads j, for every causally visible key s <= pos_offset + t, with the
+//    top-k ordered by score descending and ties going to the lower key index.
+//  * "DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다", section 두 가지 핵심 정확성 수정 사항
+//    (FP8 형식 불일치): the indexer key cache is FP8 E4M3. Here it is the OCP E4M3FN encoding
+//    (largest finite 448) with one fp32 scale per key; kscale multiplies the head sum.
+//
+// Everything is fp64: bf16, E4M3 and fp32 inputs are decoded exactly, every product and sum is
+// a double, and the selection is a full std::sort of the visible row. Memory is O(S) per thread.
+// Built with -ffp-contract=off so x86 and Arm hosts round identically.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <utility>
+#include <vector>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+namespace {
+
+enum { ORACLE_BF16 = 0, ORACLE_FP8_E4M3 = 1 };
+
+// bf16 is the top half of an IEEE binary32; widening it is exact.
+double decode_bf16(uint16_t bits) {
+  uint32_t u = static_cast<uint32_t>(bits) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+// OCP FP8 E4M3FN: 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+// S.1111.111 is NaN. Exponent field 0 encodes subnormals m/8 * 2^-6.
+double decode_e4m3(uint8_t code) {
+  const int sign = code >> 7;
+  const int e = (code >> 3) & 0xF;
+  const int m = code & 0x7;
+  if (e == 0xF && m == 0x7) return std::nan("");
+  double mag = (e == 0) ? std::ldexp(static_cast<double>(m) / 8.0, -6)
+                        : std::ldexp(1.0 + static_cast<double>(m) / 8.0, e - 7);
+  return sign ? -mag : mag;
+}
+
+struct Problem {
+  int dtype;
+  const void* q;        // [T, H, D] codes
+  const float* w;       // [T, H]
+  const void* k;        // [S, D] codes
+  const float* kscale;  // [S] or null (bf16)
+  int64_t T, S, H, D, pos_offset;
+};
+
+bool decode_all(const Problem& P, std::vector<double>& kd) {
+  kd.resize(static_cast<size_t>(P.S * P.D));
+  bool finite = true;
+#pragma omp parallel for schedule(static) reduction(&& : finite)
+  for (int64_t s = 0; s < P.S; ++s) {
+    for (int64_t i = 0; i < P.D; ++i) {
+      const int64_t o = s * P.D + i;
+      double v = (P.dtype == ORACLE_BF16) ? decode_bf16(static_cast<const uint16_t*>(P.k)[o])
+                                          : decode_e4m3(static_cast<const uint8_t*>(P.k)[o]);
+      finite = finite && std::isfinite(v);
+      kd[o] = v;
+    }
+  }
+  return finite;
+}
+
+// Number of keys query row t can see: s in [0, min(pos_offset + t, S - 1)].
+int64_t visible(const Problem& P, int64_t t) {
+  const int64_t p = P.pos_offset + t;
+  return std::min(p, P.S - 1) + 1;
+}
+
+// Scores of one query row against its visible keys, in fp64. Returns false on a non-finite input.
+bool score_row(const Problem& P, const std::vector<double>& kd, int64_t t, std::vector<double>& row) {
+  const int64_t n = visible(P, t);
+  std::vector<double> qd(static_cast<size_t>(P.H * P.D));
+  for (int64_t o = 0; o < P.H * P.D; ++o) {
+    const int64_t g = t * P.H * P.D + o;
+    qd[o] = (P.dtype == ORACLE_BF16) ? decode_bf16(static_cast<const uint16_t*>(P.q)[g])
+                                     : decode_e4m3(static_cast<const uint8_t*>(P.q)[g]);
+    if (!std::isfinite(qd[o])) return false;
+  }
+  for (int64_t j = 0; j < P.H; ++j)
+    if (!std::isfinite(P.w[t * P.H + j])) return false;
+  row.assign(static_cast<size_t>(n), 0.0);
+  for (int64_t s = 0; s < n; ++s) {
+    const double* ks = &kd[static_cast<size_t>(s * P.D)];
+    double head_sum = 0.0;
+    for (int64_t j = 0; j < P.H; ++j) {
+      const double* qj = &qd[static_cast<size_t>(j * P.D)];
+      double dot = 0.0;
+      for (int64_t i = 0; i < P.D; ++i) dot += qj[i] * ks[i];
+      const double relu = dot > 0.0 ? dot : 0.0;
+      head_sum += static_cast<double>(P.w[t * P.H + j]) * relu;
+    }
+    const double scale = (P.dtype == ORACLE_BF16) ? 1.0 : static_cast<double>(P.kscale[s]);
+    row[s] = scale * head_sum;
+  }
+  return true;
+}
+
+bool check_problem(const Problem& P) {
+  if (!P.q || !P.w || !P.k) return false;
+  if (P.dtype != ORACLE_BF16 && P.dtype != ORACLE_FP8_E4M3) return false;
+  if (P.dtype == ORACLE_FP8_E4M3 && !P.kscale) return false;
+  if (P.T < 0 || P.S < 1 || P.H < 1 || P.D < 1 || P.pos_offset < 0) return false;
+  if (P.dtype == ORACLE_FP8_E4M3)
+    for (int64_t s = 0; s < P.S; ++s)
+      if (!std::isfinite(P.kscale[s]) || P.kscale[s] < 0.f) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+// Returns the number of OpenMP threads the oracle will use (1 without OpenMP).
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
+
+// Dense fp64 scores for the listed query rows: out[r, s] = I[rows[r], s] for visible s, and
+// -inf for s beyond the row's causal limit. out is [n_rows, S]. Returns 0, or -1 on bad input.
+int oracle_scores(int dtype, const void* q, const float* w, const void* k, const float* kscale,
+                  int64_t T, int64_t S, int64_t H, int64_t D, int64_t pos_offset,
+                  const int64_t* rows, int64_t n_rows, double* out) {
+  Problem P{dtype, q, w, k, kscale, T, S, H, D, pos_offset};
+  if (!check_problem(P) || !out || (n_rows > 0 && !rows)) return -1;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= T) return -1;
+  std::vector<double> kd;
+  if (!decode_all(P, kd)) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    std::vector<double> row;
+    if (!score_row(P, kd, rows[r], row)) { bad = 1; continue; }
+    double* o = out + r * S;
+    for (int64_t s = 0; s < S; ++s)
+      o[s] = s < static_cast<int64_t>(row.size()) ? row[s] : -INFINITY;
+  }
+  return bad ? -1 : 0;
+}
+
+// Top-k of the listed query rows. For each row: order the visible (I[s], s) pairs by I
+// descending, then s ascending, keep the first m = min(topk, visible) in that order, and pad
+// slots m..topk-1 with (-1, -inf). out_idx / out_score are [n_rows, topk].
+int oracle_topk(int dtype, const void* q, const float* w, const void* k, const float* kscale,
+                int64_t T, int64_t S, int64_t H, int64_t D, int64_t pos_offset, int64_t topk,
+                const int64_t* rows, int64_t n_rows, int32_t* out_idx, double* out_score) {
+  Problem P{dtype, q, w, k, kscale, T, S, H, D, pos_offset};
+  if (!check_problem(P) || topk < 1 || !out_idx || !out_score || (n_rows > 0 && !rows)) return -1;
+  for (int64_t r = 0; r < n_rows; ++r)
+    if (rows[r] < 0 || rows[r] >= T) return -1;
+  std::vector<double> kd;
+  if (!decode_all(P, kd)) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (int64_t r = 0; r < n_rows; ++r) {
+    std::vector<double> row;
+    if (!score_row(P, kd, rows[r], row)) { bad = 1; continue; }
+    std::vector<std::pair<double, int64_t>> order(row.size());
+    for (size_t s = 0; s < row.size(); ++s) order[s] = {row[s], static_cast<int64_t>(s)};
+    std::sort(order.begin(), order.end(), [](const auto& a, const auto& b) {
+      if (a.first != b.first) return a.first > b.first;
+      return a.second < b.second;
+    });
+    const int64_t m = std::min<int64_t>(topk, static_cast<int64_t>(order.size()));
+    for (int64_t i = 0; i < topk; ++i) {
+      out_idx[r * topk + i] = i < m ? static_cast<int32_t>(order[i].second) : -1;
+      out_score[r * topk + i] = i < m ? order[i].first : -INFINITY;
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+// Exact decoders, exported so tests can pin them against closed forms and library casts.
+double oracle_decode_bf16(uint16_t bits) { return decode_bf16(bits); }
+double oracle_decode_e4m3(uint8_t code) { return decode_e4m3(code); }
+
+}  // extern "C"
