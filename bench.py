@@ -1,0 +1,396 @@
+"""Benchmark of the Lightning Indexer: query-tokens/s of one Top-512 indexer call.
+
+Default workload: cold prefill at 64k context, T = S = 65536 bf16 queries/keys, 64 index heads
+of width 128, fp32 head weights, causal, Top-512, seed 2. One step = one ds4idx_score_topk call
+(scorer + streaming Top-512, the whole path) over the full workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line. `value` is device-resident throughput (inputs already in HBM); `e2e`
+repeats the measurement through the same C-ABI call with pinned HOST buffers, the host->device
+copies of q, w and the key cache and the device->host copy of the outputs inside the timed
+region. `roofline` reports the kernel against the measured dense bf16 tensor peak (tensor-bound
+workloads) or HBM bandwidth (decode). `cpu_baseline` times the fp64 CPU oracle (test
+infrastructure, untuned) on a bounded row sample of the same workload on this host's cores.
+`--impl reference` times only that oracle, as the reference arm.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload (the indexer has no
+exchange step); value = all ranks' query tokens / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from sparse_attention_lightning_indexer_gb300 import inputs  # noqa: E402
+
+METRIC = "indexer query-tokens/s at 64k ctx (top-512) and % of tensor/HBM roofline"
+UNIT = "query-tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 / 2.25 PFLOP/s)
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "sparse_attention_lightning_indexer_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_sources") != kernel_sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+def algorithmic(prob):
+    """Causal flops (visible pairs only) and key-cache bytes of one call."""
+    T, S, pos = prob.T, prob.S, prob.pos_offset
+    t = np.arange(T, dtype=np.float64)
+    pairs = float(np.minimum(pos + t, S - 1).sum() + T)
+    flops = 2.0 * inputs.H_I * inputs.D_I * pairs
+    row_bytes = inputs.D_I * (2 if prob.dtype == inputs.BF16 else 1)
+    key_bytes = float(S * row_bytes + (S * 4 if prob.dtype == inputs.FP8_E4M3 else 0))
+    return flops, key_bytes, pairs
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running (200 ms period)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def cpu_baseline(prob, budget_s=10.0, seed=0):
+    """Times the fp64 oracle on a bounded, evenly spread row sample of `prob`."""
+    from oracle import oracle as orc
+    q, k = prob.codes()
+    ks = None if prob.kscale is None else prob.kscale.numpy()
+    w = prob.w.numpy()
+    threads = orc.num_threads()
+    # calibration: a few rows spread over the sequence
+    n_rows = max(1, min(prob.T, threads))
+    rows = np.linspace(0, prob.T - 1, n_rows).round().astype(np.int64)
+    t0 = time.perf_counter()
+    orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, rows)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n_rows = int(min(prob.T, max(n_rows, n_rows * budget_s / dt)))
+    rows = np.unique(np.linspace(0, prob.T - 1, n_rows).round().astype(np.int64))
+    t0 = time.perf_counter()
+    orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, rows)
+    dt = time.perf_counter() - t0
+    return {"value": len(rows) / dt, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"{len(rows)} query rows evenly spread over t in [0, {prob.T}) of "
+                      f"{prob.name} (full causal rows, fp64 scores + full sort), {dt:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the fp64 CPU oracle, timed on this host's cores (rank 0 only)."""
+    if rank != 0:
+        return
+    prob = inputs.workload(args.workload)
+    from oracle import oracle as orc
+    q, k = prob.codes()
+    ks = None if prob.kscale is None else prob.kscale.numpy()
+    w = prob.w.numpy()
+    threads = orc.num_threads()
+    rng = np.random.default_rng(0)
+    per_step = max(threads, 16)
+    times = []
+    done = 0
+    for step in range(args.warmup + args.steps):
+        rows = np.sort(rng.integers(0, prob.T, size=per_step))
+        t0 = time.perf_counter()
+        orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, rows)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            done += len(rows)
+    total = sum(times)
+    value = done / total
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic",
+           "config": {"workload": prob.name, "T": prob.T, "S": prob.S, "H_I": inputs.H_I,
+                      "d_I": inputs.D_I, "topk": prob.topk, "pos_offset": prob.pos_offset},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                            "sample": f"{per_step} random query rows per step of {prob.name}"},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    from sparse_attention_lightning_indexer_gb300 import ds4idx
+    from sparse_attention_lightning_indexer_gb300 import build as _build
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0 or not _build.up_to_date():
+        if world == 1 or rank == 0:
+            _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ds4idx.load()
+
+    prob = inputs.workload(args.workload)
+    dev = torch.device("cuda", local_rank)
+    log(f"[rank {rank}] workload {prob.name}: T={prob.T} S={prob.S} dtype={prob.dtype}")
+    q = prob.q.to(dev)
+    w = prob.w.to(dev)
+    k = prob.k.to(dev)
+    ks = None if prob.kscale is None else prob.kscale.to(dev)
+    ix = ds4idx.Indexer(prob.dtype, max_T=prob.T, max_S=prob.S)
+    stream = torch.cuda.current_stream()
+    out_idx = torch.empty((prob.T, prob.topk), dtype=torch.int32, device=dev)
+    out_sc = torch.empty((prob.T, prob.topk), dtype=torch.float32, device=dev)
+
+    def step():
+        ix.score_topk(q, w, k, ks, prob.pos_offset, out_idx, out_sc, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ix.sync_status()
+
+    # ---- device-resident timing: K steps between two events, barrier + sync on both sides
+    per_launch = []
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+        ev0.record(stream)
+        marks[0].record(stream)
+        for i in range(args.steps):
+            step()
+            marks[i + 1].record(stream)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = ev0.elapsed_time(ev1)
+        per_launch = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
+    ix.sync_status()
+    t_max = total_ms
+    if world > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    ms_per_step = t_max / args.steps
+    value = world * prob.T * args.steps / (t_max / 1000.0)
+
+    # ---- end to end through the C ABI with pinned host buffers
+    hq = prob.q.pin_memory()
+    hw = prob.w.pin_memory()
+    hk = prob.k.pin_memory()
+    hks = None if prob.kscale is None else prob.kscale.pin_memory()
+    ho_idx = torch.empty((prob.T, prob.topk), dtype=torch.int32).pin_memory()
+    ho_sc = torch.empty((prob.T, prob.topk), dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hw, hk) + ((hks,) if hks is not None else ()))
+    d2h = ho_idx.numel() * 4 + ho_sc.numel() * 4
+
+    def e2e_step():
+        q.copy_(hq, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        k.copy_(hk, non_blocking=True)
+        if ks is not None:
+            ks.copy_(hks, non_blocking=True)
+        ix.score_topk(q, w, k, ks, prob.pos_offset, out_idx, out_sc, stream=stream)
+        ho_idx.copy_(out_idx, non_blocking=True)
+        ho_sc.copy_(out_sc, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    ix.sync_status()
+    e2e_value = world * prob.T * e2e_steps / (e2e_ms / 1000.0)
+
+    # ---- spot parity check of a few rows against the oracle (outside every timed region)
+    spot = "skipped"
+    if rank == 0:
+        try:
+            sys.path.insert(0, os.path.join(ROOT, "tests"))
+            from tests import parity
+            rows = [0, prob.T // 3, prob.T - 1]
+            gi = out_idx.cpu().numpy()[rows]
+            gs = out_sc.cpu().numpy()[rows]
+            parity.check_rows(prob, rows, gi, gs)
+            spot = f"{len(rows)} rows match the oracle"
+        except AssertionError as e:  # reported, never hidden
+            spot = f"MISMATCH: {e}"
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        ix.close()
+        return
+
+    flops, key_bytes, pairs = algorithmic(prob)
+    peaks, peak_src = load_peaks()
+    avg_launch_ms = statistics.mean(per_launch)
+    launches_per_step = 1  # single sequence with T > 1 and enough query blocks: no split merge
+    if prob.T == 1:
+        launches_per_step = 2
+    if prob.dtype == inputs.BF16:
+        peak = peaks["bf16_tflops"]
+        peak_note = f"bf16 dense, {peak_src} (burst)"
+    else:
+        peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+        peak_note = f"fp8 dense = {peak_src} bf16 burst x {FP8_OVER_BF16} (nominal ratio)"
+    achieved = flops / (avg_launch_ms / 1000.0) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": traffic_for(prob.name),
+                "peak_source": peak_note,
+                "algorithmic": f"{flops:.4g} flop = 2*64*128 * {pairs:.4g} visible pairs",
+                "hbm_gbs_key_cache": key_bytes / (avg_launch_ms / 1000.0) / 1e9}
+    cpu = cpu_baseline(prob, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
+    out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "bf16" if prob.dtype == inputs.BF16 else "fp8_e4m3",
+           "data": "synthetic",
+           "config": {"workload": prob.name, "T": prob.T, "S": prob.S, "H_I": inputs.H_I,
+                      "d_I": inputs.D_I, "topk": prob.topk, "pos_offset": prob.pos_offset,
+                      "seed": prob.meta.get("seed"),
+                      "l2": "inputs larger than L2 (q is %.0f MiB)" % (
+                          prob.q.numel() * prob.q.element_size() / 2**20),
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+           "roofline": roofline,
+           "cpu_baseline": cpu,
+           "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+           "gpu_launches": launches_per_step * args.steps,
+           "clocks": clk.summary(),
+           "parity_spot_check": spot}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    ix.close()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="prefill_64k", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle time for cpu_baseline (0 disables)")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        log("warmup raised to 3 (minimum)")
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,129 @@
+/*
+ * ds4idx — Lightning Indexer for DeepSeek-V4-style sparse attention on GB300 (sm_103a).
+ *
+ * The operation. "DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화" (aitrends), sections
+ * 섹션별 상세 and 용어 해설, describes the Lightning Indexer as the kernel that picks, for every
+ * query token, the key positions sparse attention will read, with a Top-512 selection after a
+ * scorer. The pages print no formula; the score computed here is the DeepSeek indexer score
+ *
+ *     I[t,s] = kscale[s] * sum_{j < H_I} w[t,j] * max(0, sum_{i < d_I} q[t,j,i] * k[s,i])
+ *
+ * over H_I = 64 index heads of width d_I = 128, for every causally visible key
+ * s <= p(t) = pos_offset + t (a token sees itself), with kscale[s] = 1 for bf16 caches. For each
+ * query the library returns the top-k (k = 512) keys ordered by score descending, ties going to
+ * the lower key index; when fewer than k keys are visible, all of them are returned and the
+ * remaining slots are (-1, -inf). "DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다", section
+ * 두 가지 핵심 정확성 수정 사항 (FP8 형식 불일치), gives the FP8 E4M3 indexer key cache; here
+ * it is OCP E4M3FN (largest finite 448) with one fp32 scale per key.
+ *
+ * Arithmetic: products of bf16 (or E4M3) operands accumulate in fp32 on the tensor cores; the
+ * ReLU, the weighted head sum and the key scale are fp32. Scores match an fp64 evaluation within
+ * 1e-4 * (1 + |I|) for bf16 inputs.
+ *
+ * Conventions for every entry point:
+ *  - All tensor arguments are DEVICE pointers on the current CUDA device, row-major, dense,
+ *    16-byte aligned, owned by the caller. Nothing is copied or retained after the call.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are asynchronous: they
+ *    enqueue kernels on `stream` and return; outputs are valid once the stream has reached that
+ *    point. No entry point synchronises the host except ds4idx_sync_status and ds4idx_destroy.
+ *  - A handle is not thread-safe: use one handle per stream / host thread. The handle owns a
+ *    small device workspace (error word, per-split candidate lists) allocated at create; the
+ *    compute entry points allocate nothing.
+ *  - Return value: DS4IDX_OK (0) or a negative ds4idx_status. Argument errors are detected on
+ *    the host before anything is enqueued. Inputs must be finite (not checked on the device).
+ */
+#ifndef DS4IDX_H_
+#define DS4IDX_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DS4IDX_OK = 0,
+  DS4IDX_ERR_INVALID_ARG = -1,    /* null pointer, misalignment, size out of range, mismatch */
+  DS4IDX_ERR_UNSUPPORTED = -2,    /* shape/dtype not built (H_I != 64, d_I != 128, k != 512),
+                                     or the current device is not sm_103 */
+  DS4IDX_ERR_ALLOC = -3,          /* workspace allocation failed at create */
+  DS4IDX_ERR_LAUNCH = -4,         /* a kernel launch or an enqueue failed */
+  DS4IDX_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up on a bounded device-side wait */
+  DS4IDX_ERR_CUDA = -6            /* another CUDA runtime or driver call failed */
+} ds4idx_status;
+
+typedef enum { DS4IDX_BF16 = 0, DS4IDX_FP8_E4M3 = 1 } ds4idx_dtype;
+
+typedef struct {
+  int32_t n_heads;   /* H_I; must be 64 */
+  int32_t head_dim;  /* d_I; must be 128 */
+  int32_t topk;      /* k; must be 512 */
+  int32_t dtype;     /* ds4idx_dtype of q and kcache */
+  int64_t max_T;     /* largest query count per sequence passed to any call (>= 1) */
+  int64_t max_S;     /* largest key count per sequence (>= 1, < 2^31) */
+  int64_t max_batch; /* largest B for ds4idx_score_topk_batched (1..64) */
+} ds4idx_config;
+
+typedef struct ds4idx_handle* ds4idx_t;
+
+/* Creates a handle for the current CUDA device and allocates its workspace.
+ * Errors: INVALID_ARG (null out/cfg, ranges), UNSUPPORTED (shape or device), ALLOC, CUDA.
+ * On error *out is set to NULL. */
+int ds4idx_create(ds4idx_t* out, const ds4idx_config* cfg);
+
+/* Scores and selects for one sequence.
+ *  q         [T, 64, 128]  bf16, or E4M3 codes (uint8) for FP8 handles. For FP8 the per-token q
+ *                          scale is folded into w by the caller (w[t,j] * qscale[t]); this is exact
+ *                          because ReLU is positively homogeneous.
+ *  w         [T, 64]       fp32 head weights.
+ *  kcache    [S, 128]      bf16, or E4M3 codes for FP8 handles.
+ *  kscale    [S]           fp32 per-key scale (>= 0) for FP8; must be NULL for bf16.
+ *  T         number of query tokens (0 <= T <= max_T; T = 0 is a no-op).
+ *  S         number of keys in the cache (1 <= S <= max_S).
+ *  pos_offset position of query 0 (>= 0); query t sits at p(t) = pos_offset + t and sees keys
+ *            0..min(p(t), S - 1). A well-formed prefill or decode call has pos_offset + T <= S
+ *            (every query's own key is in the cache); positions past the cache see all S keys.
+ *  topk      must equal the handle's topk (512).
+ *  out_idx   [T, topk] int32, written: key indices, best first; -1 in unused slots.
+ *  out_score [T, topk] fp32, written: the scores of out_idx (-inf in unused slots); may be NULL.
+ */
+int ds4idx_score_topk(ds4idx_t h, const void* q, const float* w, const void* kcache,
+                      const float* kscale, int64_t T, int64_t S, int64_t pos_offset, int32_t topk,
+                      int32_t* out_idx, float* out_score, void* stream);
+
+/* B independent sequences in one launch (batched decode or chunked prefill). Every array gains
+ * a leading [B] dimension with a dense stride: q [B, T, 64, 128], w [B, T, 64],
+ * kcache [B, S, 128], kscale [B, S] (FP8), out_idx / out_score [B, T, topk].
+ * pos_offsets is a HOST array of B positions (>= 0), one per sequence.
+ * 1 <= B <= max_batch. Other arguments as in ds4idx_score_topk. */
+int ds4idx_score_topk_batched(ds4idx_t h, int32_t B, const void* q, const float* w,
+                              const void* kcache, const float* kscale, int64_t T, int64_t S,
+                              const int64_t* pos_offsets, int32_t topk, int32_t* out_idx,
+                              float* out_score, void* stream);
+
+/* Debug/test entry: the fp32 scores the selection kernels see, before selection.
+ * out_scores [T, S] fp32, written: I[t,s] for visible s, -inf for s > p(t). Same inputs and
+ * rules as ds4idx_score_topk; it runs the same scoring code path. */
+int ds4idx_score_dense_debug(ds4idx_t h, const void* q, const float* w, const void* kcache,
+                             const float* kscale, int64_t T, int64_t S, int64_t pos_offset,
+                             float* out_scores, void* stream);
+
+/* Synchronises `stream`, then reads and clears the handle's device error word.
+ * Returns DEVICE_TIMEOUT if any kernel since the last check gave up on a bounded wait
+ * (its outputs are then undefined), CUDA if the synchronisation reported an error, else OK. */
+int ds4idx_sync_status(ds4idx_t h, void* stream);
+
+/* Synchronises the device, frees the workspace and the handle. NULL is accepted (no-op). */
+int ds4idx_destroy(ds4idx_t h);
+
+/* Static English text for a status code. Never NULL. */
+const char* ds4idx_status_string(int status);
+
+/* Library ABI version: (major << 16) | minor. */
+int ds4idx_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DS4IDX_H_ */

@@ -1,0 +1,340 @@
+// Host side of the ds4idx C ABI: argument validation, TMA descriptor encoding, work
+// decomposition (query blocks x key splits) and kernel launches. Semantics of every entry point
+// are documented in include/ds4idx.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "ds4idx.h"
+#include "indexer_kernel.cuh"
+
+using namespace ds4;
+
+struct ds4idx_handle {
+  ds4idx_config cfg;
+  int device = 0;
+  int num_sms = 0;
+  uint32_t* err = nullptr;        // device error word
+  uint64_t* partial = nullptr;    // per-split Top-512 lists
+  size_t partial_words = 0;
+};
+
+namespace {
+
+constexpr int kVersion = (1 << 16) | 0;
+constexpr int kMaxSplits = 64;
+constexpr int kMinTilesPerSplit = 4;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int queries_per_cta(int64_t T) { return T == 1 ? 1 : 4; }
+
+// Work decomposition. Long sequences give plenty of CTAs from query blocks alone; short ones
+// (decode, small chunks) also split the key range so every SM gets work, and a second kernel
+// merges the per-split lists.
+struct Plan {
+  int nq = 4;
+  int n_qb = 0;
+  int n_splits = 1;
+  int tiles_per_split = 0;
+  int64_t grid = 0;
+};
+
+Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
+  Plan pl;
+  pl.nq = queries_per_cta(T);
+  pl.n_qb = static_cast<int>((T + pl.nq - 1) / pl.nq);
+  const int64_t tiles = (max_vis + kTileKeys - 1) / kTileKeys;
+  const int64_t blocks = B * pl.n_qb;
+  const int64_t target = 4LL * num_sms;
+  int64_t splits = 1;
+  if (blocks < target) {
+    splits = (target + blocks - 1) / blocks;
+    splits = std::min<int64_t>(splits, kMaxSplits);
+    splits = std::min<int64_t>(splits, std::max<int64_t>(1, tiles / kMinTilesPerSplit));
+  }
+  pl.tiles_per_split = static_cast<int>((tiles + splits - 1) / splits);
+  pl.n_splits = static_cast<int>((tiles + pl.tiles_per_split - 1) / pl.tiles_per_split);
+  if (pl.n_splits < 1) pl.n_splits = 1;
+  pl.grid = blocks * pl.n_splits;
+  return pl;
+}
+
+size_t plan_partial_words(const Plan& pl, int64_t B, int64_t T) {
+  return pl.n_splits > 1 ? static_cast<size_t>(B * T) * pl.n_splits * kTopK : 0;
+}
+
+template <int DT, int NQ, bool DENSE>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(indexer_kernel<DT, NQ, DENSE>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              KCfg<DT, NQ, DENSE>::kSmemBytes);
+}
+
+// Tensor map over `rows` rows of 128 elements per batch entry: dims {128, rows, B}.
+bool encode_rows(CUtensorMap* map, const void* base, int dtype, int64_t rows, int64_t B,
+                 int box_rows) {
+  const bool bf16 = dtype == DS4IDX_BF16;
+  const cuuint64_t row_bytes = bf16 ? 256 : 128;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDim), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(B)};
+  cuuint64_t strides[2] = {row_bytes, row_bytes * static_cast<cuuint64_t>(rows)};
+  cuuint32_t box[3] = {bf16 ? 64u : 128u, static_cast<cuuint32_t>(box_rows), 1u};
+  cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                              3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int DT, int NQ, bool DENSE>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const KParams& kp, int64_t grid,
+                   cudaStream_t stream) {
+  using C = KCfg<DT, NQ, DENSE>;
+  indexer_kernel<DT, NQ, DENSE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes,
+                                  stream>>>(tq, tk, kp);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_dt(int nq, bool dense, const CUtensorMap& tq, const CUtensorMap& tk,
+                      const KParams& kp, int64_t grid, cudaStream_t stream) {
+  if (dense) return nq == 1 ? launch<DT, 1, true>(tq, tk, kp, grid, stream)
+                            : launch<DT, 4, true>(tq, tk, kp, grid, stream);
+  if (nq == 1) return launch<DT, 1, false>(tq, tk, kp, grid, stream);
+  return launch<DT, 4, false>(tq, tk, kp, grid, stream);
+}
+
+// Shared implementation of the three compute entry points.
+int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache,
+        const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
+        int32_t* out_idx, float* out_score, float* dense, void* stream_ptr) {
+  if (!h) return DS4IDX_ERR_INVALID_ARG;
+  const ds4idx_config& c = h->cfg;
+  if (B < 1 || B > c.max_batch || B > kMaxBatch) return DS4IDX_ERR_INVALID_ARG;
+  if (T < 0 || T > c.max_T || S < 1 || S > c.max_S) return DS4IDX_ERR_INVALID_ARG;
+  if (!pos_offsets) return DS4IDX_ERR_INVALID_ARG;
+  if (!dense && topk != c.topk) return DS4IDX_ERR_INVALID_ARG;
+  if (T == 0) return DS4IDX_OK;
+  if (!q || !w || !kcache || !aligned16(q) || !aligned16(w) || !aligned16(kcache))
+    return DS4IDX_ERR_INVALID_ARG;
+  if (c.dtype == DS4IDX_FP8_E4M3) {
+    if (!kscale || (reinterpret_cast<uintptr_t>(kscale) & 3u)) return DS4IDX_ERR_INVALID_ARG;
+  } else if (kscale) {
+    return DS4IDX_ERR_INVALID_ARG;
+  }
+  if (dense) {
+    if (!aligned16(dense)) return DS4IDX_ERR_INVALID_ARG;
+  } else {
+    if (!out_idx || !aligned16(out_idx)) return DS4IDX_ERR_INVALID_ARG;
+    if (out_score && !aligned16(out_score)) return DS4IDX_ERR_INVALID_ARG;
+  }
+  int64_t max_vis = 0;
+  for (int b = 0; b < B; ++b) {
+    if (pos_offsets[b] < 0 || pos_offsets[b] > (1LL << 40)) return DS4IDX_ERR_INVALID_ARG;
+    max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
+  }
+  if (T * kHeads > (1LL << 31) - 1) return DS4IDX_ERR_INVALID_ARG;
+  if (!load_encode()) return DS4IDX_ERR_CUDA;
+
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return DS4IDX_ERR_INVALID_ARG;
+
+  Plan pl = make_plan(h->num_sms, B, T, max_vis);
+  if (dense) {
+    // Same query blocking as the Top-k path, so the debug scores come from identical MMA tiles.
+    pl.nq = queries_per_cta(T);
+    pl.n_qb = static_cast<int>((T + pl.nq - 1) / pl.nq);
+    pl.n_splits = 1;
+    pl.tiles_per_split = static_cast<int>((S + kTileKeys - 1) / kTileKeys);
+    pl.grid = pl.n_qb;
+  }
+  if (plan_partial_words(pl, B, T) > h->partial_words) return DS4IDX_ERR_INVALID_ARG;
+
+  CUtensorMap tq, tk;
+  if (!encode_rows(&tq, q, c.dtype, T * kHeads, B, kHeads * pl.nq)) return DS4IDX_ERR_INVALID_ARG;
+  if (!encode_rows(&tk, kcache, c.dtype, S, B, kTileKeys)) return DS4IDX_ERR_INVALID_ARG;
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof kp);
+  kp.w = w;
+  kp.kscale = kscale;
+  kp.out_idx = out_idx;
+  kp.out_score = out_score;
+  kp.partial = h->partial;
+  kp.dense = dense;
+  kp.err = h->err;
+  kp.T = T;
+  kp.S = S;
+  kp.B = B;
+  kp.n_qb = pl.n_qb;
+  kp.n_splits = pl.n_splits;
+  kp.tiles_per_split = pl.tiles_per_split;
+  for (int b = 0; b < B; ++b) kp.pos[b] = pos_offsets[b];
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  cudaError_t e = c.dtype == DS4IDX_BF16
+                      ? launch_dt<kDtBf16>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream)
+                      : launch_dt<kDtFp8>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream);
+  if (e != cudaSuccess) return DS4IDX_ERR_LAUNCH;
+  if (!dense && pl.n_splits > 1) {
+    const int64_t rows = static_cast<int64_t>(B) * T;
+    merge_splits_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
+        h->partial, pl.n_splits, rows, out_idx, out_score);
+    if (cudaGetLastError() != cudaSuccess) return DS4IDX_ERR_LAUNCH;
+  }
+  return DS4IDX_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ds4idx_version(void) { return kVersion; }
+
+const char* ds4idx_status_string(int status) {
+  switch (status) {
+    case DS4IDX_OK: return "ok";
+    case DS4IDX_ERR_INVALID_ARG: return "invalid argument";
+    case DS4IDX_ERR_UNSUPPORTED: return "unsupported shape, dtype or device";
+    case DS4IDX_ERR_ALLOC: return "device workspace allocation failed";
+    case DS4IDX_ERR_LAUNCH: return "kernel launch failed";
+    case DS4IDX_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded device wait";
+    case DS4IDX_ERR_CUDA: return "CUDA runtime or driver error";
+    default: return "unknown status";
+  }
+}
+
+int ds4idx_create(ds4idx_t* out, const ds4idx_config* cfg) {
+  if (!out) return DS4IDX_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!cfg) return DS4IDX_ERR_INVALID_ARG;
+  if (cfg->dtype != DS4IDX_BF16 && cfg->dtype != DS4IDX_FP8_E4M3) return DS4IDX_ERR_INVALID_ARG;
+  if (cfg->max_T < 1 || cfg->max_S < 1 || cfg->max_S > (1LL << 31) - 1 || cfg->max_batch < 1 ||
+      cfg->max_batch > kMaxBatch)
+    return DS4IDX_ERR_INVALID_ARG;
+  if (cfg->n_heads != kHeads || cfg->head_dim != kDim || cfg->topk != kTopK)
+    return DS4IDX_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS4IDX_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return DS4IDX_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return DS4IDX_ERR_UNSUPPORTED;
+  if (!load_encode()) return DS4IDX_ERR_CUDA;
+
+  if (set_smem_attr<kDtBf16, 4, false>() != cudaSuccess ||
+      set_smem_attr<kDtBf16, 1, false>() != cudaSuccess ||
+      set_smem_attr<kDtBf16, 4, true>() != cudaSuccess ||
+      set_smem_attr<kDtBf16, 1, true>() != cudaSuccess ||
+      set_smem_attr<kDtFp8, 1, true>() != cudaSuccess ||
+      set_smem_attr<kDtFp8, 4, false>() != cudaSuccess ||
+      set_smem_attr<kDtFp8, 1, false>() != cudaSuccess ||
+      set_smem_attr<kDtFp8, 4, true>() != cudaSuccess)
+    return DS4IDX_ERR_CUDA;
+
+  ds4idx_handle* h = new (std::nothrow) ds4idx_handle();
+  if (!h) return DS4IDX_ERR_ALLOC;
+  h->cfg = *cfg;
+  h->device = dev;
+  h->num_sms = prop.multiProcessorCount;
+
+  // Workspace for the largest per-split candidate set any admissible call can need.
+  size_t words = 0;
+  for (int64_t B = 1; B <= cfg->max_batch; ++B) {
+    const int64_t t_hi = std::min<int64_t>(cfg->max_T, 16LL * h->num_sms);
+    for (int64_t T = 1; T <= t_hi; ++T) {
+      const Plan pl = make_plan(h->num_sms, B, T, cfg->max_S);
+      words = std::max(words, plan_partial_words(pl, B, T));
+    }
+  }
+  h->partial_words = words;
+  if (cudaMalloc(&h->err, 16) != cudaSuccess) {
+    delete h;
+    return DS4IDX_ERR_ALLOC;
+  }
+  if (words && cudaMalloc(&h->partial, words * sizeof(uint64_t)) != cudaSuccess) {
+    cudaFree(h->err);
+    delete h;
+    return DS4IDX_ERR_ALLOC;
+  }
+  if (cudaMemset(h->err, 0, 16) != cudaSuccess) {
+    cudaFree(h->partial);
+    cudaFree(h->err);
+    delete h;
+    return DS4IDX_ERR_CUDA;
+  }
+  *out = h;
+  return DS4IDX_OK;
+}
+
+int ds4idx_score_topk(ds4idx_t h, const void* q, const float* w, const void* kcache,
+                      const float* kscale, int64_t T, int64_t S, int64_t pos_offset, int32_t topk,
+                      int32_t* out_idx, float* out_score, void* stream) {
+  return run(h, 1, q, w, kcache, kscale, T, S, &pos_offset, topk, out_idx, out_score, nullptr,
+             stream);
+}
+
+int ds4idx_score_topk_batched(ds4idx_t h, int32_t B, const void* q, const float* w,
+                              const void* kcache, const float* kscale, int64_t T, int64_t S,
+                              const int64_t* pos_offsets, int32_t topk, int32_t* out_idx,
+                              float* out_score, void* stream) {
+  return run(h, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score, nullptr,
+             stream);
+}
+
+int ds4idx_score_dense_debug(ds4idx_t h, const void* q, const float* w, const void* kcache,
+                             const float* kscale, int64_t T, int64_t S, int64_t pos_offset,
+                             float* out_scores, void* stream) {
+  if (!out_scores) return DS4IDX_ERR_INVALID_ARG;
+  return run(h, 1, q, w, kcache, kscale, T, S, &pos_offset, 0, nullptr, nullptr, out_scores,
+             stream);
+}
+
+int ds4idx_sync_status(ds4idx_t h, void* stream) {
+  if (!h) return DS4IDX_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return DS4IDX_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DS4IDX_ERR_CUDA;
+  if (word) {
+    cudaMemset(h->err, 0, sizeof word);
+    return DS4IDX_ERR_DEVICE_TIMEOUT;
+  }
+  return DS4IDX_OK;
+}
+
+int ds4idx_destroy(ds4idx_t h) {
+  if (!h) return DS4IDX_OK;
+  const cudaError_t e = cudaDeviceSynchronize();
+  cudaFree(h->partial);
+  cudaFree(h->err);
+  delete h;
+  return e == cudaSuccess ? DS4IDX_OK : DS4IDX_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,387 @@
+// The Lightning Indexer kernel for sm_103a: tcgen05 scorer with a fused epilogue and a
+// streaming per-query Top-512.
+//
+// What it computes ("DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화", 섹션별 상세 / 용어 해설:
+// the indexer scores every visible key of a query and a Top-512 selection keeps the best):
+//     I[t,s] = kscale[s] * sum_j w[t,j] * max(0, q[t,j,:] . k[s,:]),  s <= pos_offset + t,
+// keeping per query the 512 largest (score, lower-index-first) pairs.
+//
+// One CTA owns NQ consecutive queries of one sequence (and, when the key range is split, one
+// slice of their keys). Its warps:
+//   warps 0..3   epilogue: warp w reads TMEM lanes 32w..32w+31, i.e. one key per thread, and
+//                reduces the 64 head columns of each query thread-locally (ReLU, * w, sum),
+//                so the T x S score matrix never leaves the SM;
+//   warp 4       TMA producer: Q block once, then 128-key K tiles into a ring of stages;
+//   warp 5       TMEM owner and MMA issuer: per key tile, D[128 keys, NQ*64 (query, head)]
+//                = K_tile . Q_block^T on tcgen05 into one of two TMEM accumulators;
+//   warps 6..    one selector warp per query: filters the tile's scores against the running
+//                threshold, buffers survivors and merges them into its sorted Top-512 list.
+// Keys are the MMA M dimension (128 = all TMEM lanes) and (query, head) pairs the N dimension,
+// which is what makes the head reduction free of shuffles. The design on the page (a
+// threadgroup-tiled scorer, then a register-blocked K-resident scorer, then a streaming
+// Top-512, on Apple GPUs) is prior art; this layout follows from TMEM's lane/column shape.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+
+#include "ptx.cuh"
+#include "topk.cuh"
+
+namespace ds4 {
+
+constexpr int kHeads = 64;       // H_I
+constexpr int kDim = 128;        // d_I
+constexpr int kTopK = 512;
+constexpr int kTileKeys = 128;   // MMA M
+constexpr int kBufCap = 256;     // per-query candidate buffer
+constexpr int kScoreBufs = 4;    // depth of the epilogue -> selector score ring
+constexpr int kMaxBatch = 64;
+constexpr int kDtBf16 = 0;
+constexpr int kDtFp8 = 1;
+
+struct KParams {
+  const float* w;        // [B, T, 64]
+  const float* kscale;   // [B, S] (FP8) or null
+  int32_t* out_idx;      // [B, T, 512]
+  float* out_score;      // [B, T, 512] or null
+  uint64_t* partial;     // [B, T, n_splits, 512] packed lists when n_splits > 1
+  float* dense;          // [T, S] scores (debug variant)
+  uint32_t* err;         // device error word
+  int64_t T, S;
+  int32_t B, n_qb, n_splits, tiles_per_split;
+  int64_t pos[kMaxBatch];
+};
+
+template <int DT, int NQ, bool DENSE>
+struct KCfg {
+  static constexpr int kRowBytes = DT == kDtBf16 ? 2 * kDim : kDim;  // one 128-dim row
+  static constexpr int kHalves = kRowBytes / 128;                    // 128-byte swizzle columns
+  static constexpr int kN = kHeads * NQ;                             // MMA N
+  static constexpr int kQBytes = kN * kRowBytes;
+  static constexpr int kKBytes = kTileKeys * kRowBytes;
+  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 6) : (NQ == 4 ? 6 : 8);
+  static constexpr int kKSteps = DT == kDtBf16 ? kDim / 16 : kDim / 32;
+  static constexpr int kStepBytes = 32;                              // K bytes per MMA step
+  static constexpr int kSelectors = DENSE ? 0 : NQ;
+  static constexpr int kWarps = 6 + kSelectors;
+  static constexpr int kThreads = 32 * kWarps;
+  static constexpr uint32_t kTmemCols = 2 * kN <= 32 ? 32 : (2 * kN <= 64 ? 64 : (2 * kN <= 128 ? 128 : (2 * kN <= 256 ? 256 : 512)));
+  static constexpr uint32_t kIdesc =
+      DT == kDtBf16 ? instr_desc(1u, 1u, kTileKeys, kN) : instr_desc(0u, 0u, kTileKeys, kN);
+  // shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kQBytes;
+  static constexpr int kOffW = kOffK + kStages * kKBytes;
+  static constexpr int kOffScore = kOffW + NQ * kHeads * 4;
+  static constexpr int kOffList = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
+  static constexpr int kOffBuf = kOffList + (DENSE ? 0 : NQ * kTopK * 8);
+  static constexpr int kOffBar = kOffBuf + (DENSE ? 0 : NQ * kBufCap * 8);
+  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kScoreBufs + 1;
+  static constexpr int kOffMisc = kOffBar + kNumBars * 8;
+  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
+};
+
+template <int DT, int NQ, bool DENSE>
+__global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                   const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ KParams p) {
+  using C = KCfg<DT, NQ, DENSE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sQ = smem + C::kOffQ;
+  uint8_t* sK = smem + C::kOffK;
+  float* sW = reinterpret_cast<float*>(smem + C::kOffW);
+  float* sScore = reinterpret_cast<float*>(smem + C::kOffScore);
+  uint64_t* sList = reinterpret_cast<uint64_t*>(smem + C::kOffList);
+  uint64_t* sBuf = reinterpret_cast<uint64_t*>(smem + C::kOffBuf);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
+  uint64_t* full = bars;                         // [kStages]  TMA -> MMA
+  uint64_t* empty = full + C::kStages;           // [kStages]  MMA -> TMA
+  uint64_t* tfull = empty + C::kStages;          // [2]        MMA -> epilogue
+  uint64_t* tempty = tfull + 2;                  // [2]        epilogue -> MMA
+  uint64_t* sfull = tempty + 2;                  // [kScoreBufs] epilogue -> selectors
+  uint64_t* sempty = sfull + kScoreBufs;         // [kScoreBufs] selectors -> epilogue
+  uint64_t* qfull = sempty + kScoreBufs;         // Q block landed
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---- work item: longest query blocks first; batches and key splits innermost
+  const int wid = blockIdx.x;
+  const int b = wid % p.B;
+  const int rest = wid / p.B;
+  const int split = rest % p.n_splits;
+  const int qb = p.n_qb - 1 - rest / p.n_splits;
+  const int64_t t0 = static_cast<int64_t>(qb) * NQ;
+  const int64_t t_last = (t0 + NQ < p.T ? t0 + NQ : p.T) - 1;
+  const int64_t pos_b = p.pos[b];
+  int tile_lo, n_tiles;
+  if (DENSE) {
+    tile_lo = 0;
+    n_tiles = static_cast<int>((p.S + kTileKeys - 1) / kTileKeys);
+  } else {
+    const int64_t p_last = pos_b + t_last;
+    const int64_t vis_end = (p_last < p.S - 1 ? p_last : p.S - 1) + 1;
+    const int tiles_total = static_cast<int>((vis_end + kTileKeys - 1) / kTileKeys);
+    tile_lo = split * p.tiles_per_split;
+    const int hi = tile_lo + p.tiles_per_split < tiles_total ? tile_lo + p.tiles_per_split
+                                                              : tiles_total;
+    n_tiles = hi > tile_lo ? hi - tile_lo : 0;
+  }
+
+  // ---- setup
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);
+    }
+    for (int i = 0; i < kScoreBufs; ++i) {
+      mbar_init(&sfull[i], 4);
+      mbar_init(&sempty[i], NQ);
+    }
+    mbar_init(qfull, 1);
+    *s_abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 4 && lane == 0) {
+    tma_prefetch_desc(&tmap_q);
+    tma_prefetch_desc(&tmap_k);
+  }
+  if (warp == 5) {
+    tmem_alloc(s_tmem, C::kTmemCols);
+    tmem_relinquish();
+  }
+  for (int i = threadIdx.x; i < NQ * kHeads; i += C::kThreads) {
+    const int64_t t = t0 + i / kHeads;
+    sW[i] = t < p.T ? p.w[(static_cast<int64_t>(b) * p.T + t) * kHeads + (i % kHeads)] : 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  if (warp == 4) {
+    // ================= TMA producer
+    if (lane == 0 && n_tiles > 0) {
+      mbar_arrive_expect_tx(qfull, C::kQBytes);
+      for (int h = 0; h < C::kHalves; ++h)
+        tma_load_3d(sQ + h * (C::kN * 128), &tmap_q, qfull, h * 64 * (DT == kDtBf16 ? 1 : 2),
+                    static_cast<int32_t>(t0 * kHeads), b);
+      int it = 0;
+      for (; it < n_tiles; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t ph = (it / C::kStages) & 1;
+        if (!mbar_wait(&empty[st], ph ^ 1u, s_abort, p.err)) break;
+        mbar_arrive_expect_tx(&full[st], C::kKBytes);
+        uint8_t* dst = sK + st * C::kKBytes;
+        const int32_t key0 = (tile_lo + it) * kTileKeys;
+        for (int h = 0; h < C::kHalves; ++h)
+          tma_load_3d(dst + h * (kTileKeys * 128), &tmap_k, &full[st],
+                      h * 64 * (DT == kDtBf16 ? 1 : 2), key0, b);
+      }
+      // Never leave the CTA with copies in flight: wait (bounded) for the last load of each
+      // stage and for the Q block. After a normal run these have long completed.
+      const int issued = it;
+      for (int j = issued - C::kStages > 0 ? issued - C::kStages : 0; j < issued; ++j)
+        mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, s_abort, p.err);
+      mbar_wait(qfull, 0, s_abort, p.err);
+    }
+  } else if (warp == 5) {
+    // ================= MMA issuer (one thread)
+    if (lane == 0 && n_tiles > 0) {
+      int it = 0;
+      bool ok = mbar_wait(qfull, 0, s_abort, p.err);
+      for (; ok && it < n_tiles; ++it) {
+        const int st = it % C::kStages;
+        const uint32_t sph = (it / C::kStages) & 1;
+        const int acc = it & 1;
+        const uint32_t aph = (it >> 1) & 1;
+        if (!mbar_wait(&full[st], sph, s_abort, p.err)) break;
+        if (!mbar_wait(&tempty[acc], aph ^ 1u, s_abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + static_cast<uint32_t>(acc * C::kN);
+        const uint32_t a_base = smem_u32(sK + st * C::kKBytes);
+        const uint32_t b_base = smem_u32(sQ);
+#pragma unroll
+        for (int ks = 0; ks < C::kKSteps; ++ks) {
+          const int half = ks / (128 / C::kStepBytes);
+          const int koff = (ks % (128 / C::kStepBytes)) * C::kStepBytes;
+          const uint64_t a_desc = smem_desc_sw128(a_base + half * (kTileKeys * 128) + koff);
+          const uint64_t b_desc = smem_desc_sw128(b_base + half * (C::kN * 128) + koff);
+          if (DT == kDtBf16)
+            mma_bf16(d, a_desc, b_desc, C::kIdesc, ks > 0 ? 1u : 0u);
+          else
+            mma_fp8(d, a_desc, b_desc, C::kIdesc, ks > 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[st]);
+        mma_commit(&tfull[it & 1]);
+      }
+      // Before TMEM is released every issued MMA must have completed: wait for the commit of
+      // the last tile issued (the epilogue waits on the same phase).
+      if (it > 0) {
+        const int last = it - 1;
+        mbar_wait(&tfull[last & 1], (last >> 1) & 1, s_abort, p.err);
+      }
+    }
+    __syncwarp();
+  } else if (warp < 4) {
+    // ================= epilogue: TMEM -> ReLU . w -> per-key score
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int acc = it & 1;
+      const uint32_t aph = (it >> 1) & 1;
+      const int sb = it % kScoreBufs;
+      const uint32_t sph = (it / kScoreBufs) & 1;
+      const int64_t key = static_cast<int64_t>(tile_lo + it) * kTileKeys + warp * 32 + lane;
+      float ks = 1.f;
+      if (DT == kDtFp8) ks = key < p.S ? p.kscale[static_cast<int64_t>(b) * p.S + key] : 0.f;
+      if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
+      tc_fence_after();
+      if (!DENSE) {
+        if (!mbar_wait_warp(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
+      }
+#pragma unroll 1
+      for (int q = 0; q < NQ; ++q) {
+        uint32_t r0[32], r1[32];
+        const uint32_t col = tmem + lane_base + static_cast<uint32_t>(acc * C::kN + q * kHeads);
+        tmem_ld32(col, r0);
+        tmem_ld32(col + 32, r1);
+        tmem_wait_ld();
+        const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads);
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wv = w4[h4];
+          a0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), a0);
+          a1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), a1);
+          a2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), a2);
+          a3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), a3);
+        }
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
+          const float4 wv = w4[8 + h4];
+          a0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), a0);
+          a1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), a1);
+          a2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), a2);
+          a3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), a3);
+        }
+        float score = (a0 + a1) + (a2 + a3);
+        if (DT == kDtFp8) score *= ks;
+        if (DENSE) {
+          const int64_t t = t0 + q;
+          if (t < p.T && key < p.S) {
+            const bool vis = key <= pos_b + t;
+            p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
+          }
+        } else {
+          sScore[(sb * NQ + q) * kTileKeys + warp * 32 + lane] = score;
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&tempty[acc]);
+        if (!DENSE) mbar_arrive(&sfull[sb]);
+      }
+    }
+  } else if (!DENSE) {
+    // ================= selector: one warp per query of the block
+    const int q = warp - 6;
+    uint64_t* list = sList + q * kTopK;
+    uint64_t* buf = sBuf + q * kBufCap;
+    for (int i = lane; i < kTopK; i += 32) list[i] = 0ull;
+    __syncwarp();
+    const int64_t t = t0 + q;
+    const bool valid = t < p.T;
+    const int64_t pt = pos_b + t;
+    const int64_t vis_end = valid ? (pt < p.S - 1 ? pt : p.S - 1) + 1 : 0;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    uint64_t theta = 0ull;
+    int nbuf = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int sb = it % kScoreBufs;
+      const uint32_t sph = (it / kScoreBufs) & 1;
+      if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
+      const int64_t key0 = static_cast<int64_t>(tile_lo + it) * kTileKeys;
+      const float* sc = sScore + (sb * NQ + q) * kTileKeys;
+#pragma unroll
+      for (int r = 0; r < kTileKeys / 32; ++r) {
+        const int64_t key = key0 + r * 32 + lane;
+        const uint64_t u = key < vis_end ? pack_key(sc[r * 32 + lane], static_cast<uint32_t>(key))
+                                         : 0ull;
+        const bool pass = u > theta;
+        const uint32_t m = __ballot_sync(0xffffffffu, pass);
+        if (pass) buf[nbuf + __popc(m & lt_mask)] = u;
+        nbuf += __popc(m);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sempty[sb]);
+      if (nbuf > kBufCap - kTileKeys) {
+        merge_buffer<kTopK, kBufCap>(list, buf, nbuf, lane);
+        theta = list[kTopK - 1];
+        nbuf = 0;
+      }
+    }
+    if (nbuf > 0) merge_buffer<kTopK, kBufCap>(list, buf, nbuf, lane);
+    __syncwarp();
+    if (valid && !*s_abort) {
+      const int64_t row = static_cast<int64_t>(b) * p.T + t;
+      if (p.n_splits > 1) {
+        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
+        for (int i = lane; i < kTopK; i += 32) dst[i] = list[i];
+      } else {
+        for (int i = lane; i < kTopK; i += 32) {
+          const uint64_t u = list[i];
+          p.out_idx[row * kTopK + i] = u ? key_index(u) : -1;
+          if (p.out_score) p.out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
+        }
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+// Combines per-split Top-512 lists (each sorted, packed) into the final output. One warp per
+// output row, pairwise bitonic merges in shared memory.
+__global__ void __launch_bounds__(128) merge_splits_kernel(const uint64_t* __restrict__ partial,
+                                                           int n_splits, int64_t n_rows,
+                                                           int32_t* __restrict__ out_idx,
+                                                           float* __restrict__ out_score) {
+  __shared__ uint64_t s_lists[4][2][kTopK];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
+  if (row >= n_rows) return;
+  uint64_t* acc = s_lists[warp][0];
+  uint64_t* nxt = s_lists[warp][1];
+  const uint64_t* src = partial + row * n_splits * kTopK;
+  for (int i = lane; i < kTopK; i += 32) acc[i] = src[i];
+  __syncwarp();
+  for (int sp = 1; sp < n_splits; ++sp) {
+    for (int i = lane; i < kTopK; i += 32) nxt[i] = src[sp * kTopK + i];
+    __syncwarp();
+    merge_lists<kTopK>(acc, nxt, lane);
+  }
+  for (int i = lane; i < kTopK; i += 32) {
+    const uint64_t u = acc[i];
+    out_idx[row * kTopK + i] = u ? key_index(u) : -1;
+    if (out_score) out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
+  }
+}
+
+}  // namespace ds4

@@ -1,0 +1,242 @@
+"""Python binding of the ds4idx C ABI (include/ds4idx.h): argument marshalling only.
+
+Every step of the indexer runs in the CUDA kernels of ``libds4idx.so``; this module checks
+tensor shapes, dtypes and devices, passes raw device pointers and the current CUDA stream, and
+turns status codes into exceptions. PyTorch provides device memory and streams. There is no
+CPU fallback: if the library is missing or the device is not sm_103, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+BF16 = 0
+FP8_E4M3 = 1
+H_I = 64
+D_I = 128
+TOPK = 512
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_ALLOC = -3
+ERR_LAUNCH = -4
+ERR_DEVICE_TIMEOUT = -5
+ERR_CUDA = -6
+
+EXPORTS = ("ds4idx_create", "ds4idx_score_topk", "ds4idx_score_topk_batched",
+           "ds4idx_score_dense_debug", "ds4idx_sync_status", "ds4idx_destroy",
+           "ds4idx_status_string", "ds4idx_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Ds4IdxError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("n_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("topk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("max_T", ctypes.c_int64), ("max_S", ctypes.c_int64),
+                ("max_batch", ctypes.c_int64)]
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def load(path: str | None = None):
+    """Loads libds4idx.so (built in-tree by ``build.build()``). Raises if it is absent."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or library_path()
+        if not os.path.exists(p):
+            raise RuntimeError(f"ds4idx library not built: {p} is missing (run build())")
+        lib = ctypes.CDLL(p)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32
+        lib.ds4idx_create.argtypes = [ctypes.POINTER(vp), ctypes.POINTER(Config)]
+        lib.ds4idx_create.restype = ctypes.c_int
+        lib.ds4idx_score_topk.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp]
+        lib.ds4idx_score_topk.restype = ctypes.c_int
+        lib.ds4idx_score_topk_batched.argtypes = [vp, i32, vp, vp, vp, vp, i64, i64, vp, i32, vp,
+                                                  vp, vp]
+        lib.ds4idx_score_topk_batched.restype = ctypes.c_int
+        lib.ds4idx_score_dense_debug.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, vp, vp]
+        lib.ds4idx_score_dense_debug.restype = ctypes.c_int
+        lib.ds4idx_sync_status.argtypes = [vp, vp]
+        lib.ds4idx_sync_status.restype = ctypes.c_int
+        lib.ds4idx_destroy.argtypes = [vp]
+        lib.ds4idx_destroy.restype = ctypes.c_int
+        lib.ds4idx_status_string.argtypes = [ctypes.c_int]
+        lib.ds4idx_status_string.restype = ctypes.c_char_p
+        lib.ds4idx_version.argtypes = []
+        lib.ds4idx_version.restype = ctypes.c_int
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().ds4idx_status_string(int(status)).decode()
+    except RuntimeError:
+        return "library not loaded"
+
+
+def _check(status: int, what: str):
+    if status != OK:
+        raise Ds4IdxError(status, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_ptr(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _codes(t: torch.Tensor, dtype: int, name: str) -> torch.Tensor:
+    if dtype == BF16:
+        if t.dtype != torch.bfloat16:
+            raise TypeError(f"{name} must be bfloat16 for a bf16 indexer")
+        return t
+    if t.dtype == torch.float8_e4m3fn:
+        return t.view(torch.uint8)
+    if t.dtype != torch.uint8:
+        raise TypeError(f"{name} must be float8_e4m3fn or uint8 E4M3 codes for an FP8 indexer")
+    return t
+
+
+def _need(t: torch.Tensor, shape, name: str, dtype=None):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}")
+
+
+class Indexer:
+    """One ds4idx handle (device workspace) for a dtype and maximum sizes."""
+
+    def __init__(self, dtype: int = BF16, max_T: int = 65536, max_S: int = 65536,
+                 max_batch: int = 1, n_heads: int = H_I, head_dim: int = D_I, topk: int = TOPK):
+        self._lib = load()
+        self.dtype = dtype
+        self.topk = topk
+        cfg = Config(n_heads, head_dim, topk, dtype, max_T, max_S, max_batch)
+        h = ctypes.c_void_p()
+        _check(self._lib.ds4idx_create(ctypes.byref(h), ctypes.byref(cfg)), "ds4idx_create")
+        self._h = h
+
+    @property
+    def handle(self):
+        return self._h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.ds4idx_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def score_topk(self, q, w, kcache, kscale=None, pos_offset: int = 0, out_idx=None,
+                   out_score=None, stream=None, want_score: bool = True):
+        """q [T,64,128], w [T,64] fp32, kcache [S,128], kscale [S] fp32 (FP8) -> (idx, score)."""
+        T, S = q.shape[0], kcache.shape[0]
+        q = _codes(q, self.dtype, "q")
+        kcache = _codes(kcache, self.dtype, "kcache")
+        _need(q, (T, H_I, D_I), "q")
+        _need(w, (T, H_I), "w", torch.float32)
+        _need(kcache, (S, D_I), "kcache")
+        if kscale is not None:
+            _need(kscale, (S,), "kscale", torch.float32)
+        dev = q.device
+        if out_idx is None:
+            out_idx = torch.empty((T, self.topk), dtype=torch.int32, device=dev)
+        if out_score is None and want_score:
+            out_score = torch.empty((T, self.topk), dtype=torch.float32, device=dev)
+        _need(out_idx, (T, self.topk), "out_idx", torch.int32)
+        if out_score is not None:
+            _need(out_score, (T, self.topk), "out_score", torch.float32)
+        st = self._lib.ds4idx_score_topk(self._h, _ptr(q), _ptr(w), _ptr(kcache), _ptr(kscale),
+                                         T, S, int(pos_offset), self.topk, _ptr(out_idx),
+                                         _ptr(out_score), _stream_ptr(stream))
+        _check(st, "ds4idx_score_topk")
+        return out_idx, out_score
+
+    def score_topk_batched(self, q, w, kcache, kscale, pos_offsets, out_idx=None, out_score=None,
+                           stream=None):
+        """q [B,T,64,128], w [B,T,64], kcache [B,S,128], kscale [B,S]; pos_offsets: B ints."""
+        B, T, S = q.shape[0], q.shape[1], kcache.shape[1]
+        q = _codes(q, self.dtype, "q")
+        kcache = _codes(kcache, self.dtype, "kcache")
+        _need(q, (B, T, H_I, D_I), "q")
+        _need(w, (B, T, H_I), "w", torch.float32)
+        _need(kcache, (B, S, D_I), "kcache")
+        if kscale is not None:
+            _need(kscale, (B, S), "kscale", torch.float32)
+        dev = q.device
+        if out_idx is None:
+            out_idx = torch.empty((B, T, self.topk), dtype=torch.int32, device=dev)
+        if out_score is None:
+            out_score = torch.empty((B, T, self.topk), dtype=torch.float32, device=dev)
+        _need(out_idx, (B, T, self.topk), "out_idx", torch.int32)
+        _need(out_score, (B, T, self.topk), "out_score", torch.float32)
+        pos = (ctypes.c_int64 * B)(*[int(x) for x in pos_offsets])
+        st = self._lib.ds4idx_score_topk_batched(self._h, B, _ptr(q), _ptr(w), _ptr(kcache),
+                                                 _ptr(kscale), T, S, ctypes.cast(pos, ctypes.c_void_p),
+                                                 self.topk, _ptr(out_idx), _ptr(out_score),
+                                                 _stream_ptr(stream))
+        _check(st, "ds4idx_score_topk_batched")
+        return out_idx, out_score
+
+    def score_dense_debug(self, q, w, kcache, kscale=None, pos_offset: int = 0, out=None,
+                          stream=None):
+        """fp32 scores [T, S] as the selection kernels see them (-inf where not visible)."""
+        T, S = q.shape[0], kcache.shape[0]
+        q = _codes(q, self.dtype, "q")
+        kcache = _codes(kcache, self.dtype, "kcache")
+        _need(q, (T, H_I, D_I), "q")
+        _need(w, (T, H_I), "w", torch.float32)
+        _need(kcache, (S, D_I), "kcache")
+        if kscale is not None:
+            _need(kscale, (S,), "kscale", torch.float32)
+        if out is None:
+            out = torch.empty((T, S), dtype=torch.float32, device=q.device)
+        _need(out, (T, S), "out", torch.float32)
+        st = self._lib.ds4idx_score_dense_debug(self._h, _ptr(q), _ptr(w), _ptr(kcache),
+                                                _ptr(kscale), T, S, int(pos_offset), _ptr(out),
+                                                _stream_ptr(stream))
+        _check(st, "ds4idx_score_dense_debug")
+        return out
+
+    def sync_status(self, stream=None):
+        _check(self._lib.ds4idx_sync_status(self._h, _stream_ptr(stream)), "ds4idx_sync_status")

@@ -1,0 +1,189 @@
+"""GPU parity: the CUDA indexer (through the C ABI) against the fp64 oracle.
+
+Sizes here are ones the oracle finishes in seconds while still spanning several 128-key tiles,
+several 4-query blocks, ragged tails of both, key-range splits and the merge kernel. Every row
+is checked with the score / set / order rules and the selection rerun on the kernel's own fp32
+scores (tests/parity.py).
+"""
+import numpy as np
+import pytest
+import torch
+
+from sparse_attention_lightning_indexer_gb300 import inputs
+from sparse_attention_lightning_indexer_gb300 import ds4idx
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def bf16_ix():
+    with ds4idx.Indexer(ds4idx.BF16, max_T=16384, max_S=65536, max_batch=8) as ix:
+        yield ix
+
+
+@pytest.fixture(scope="module")
+def fp8_ix():
+    with ds4idx.Indexer(ds4idx.FP8_E4M3, max_T=16384, max_S=65536, max_batch=8) as ix:
+        yield ix
+
+
+def _ix(prob, bf16_ix, fp8_ix):
+    return bf16_ix if prob.dtype == inputs.BF16 else fp8_ix
+
+
+def run_full(prob, ix, rerun=True):
+    dev = parity.to_device(prob)
+    idx, sc = ix.score_topk(*dev, pos_offset=prob.pos_offset)
+    ix.sync_status()
+    rows = list(range(prob.T))
+    gi, gs = idx.cpu().numpy(), sc.cpu().numpy()
+    stats = parity.check_rows(prob, rows, gi, gs)
+    if rerun:
+        dense = ix.score_dense_debug(*dev, pos_offset=prob.pos_offset).cpu().numpy()
+        parity.rerun_selection(prob, rows, dense, gi, gs)
+    return stats, gi, gs
+
+
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP8_E4M3])
+def test_ragged_prefill(dtype, bf16_ix, fp8_ix):
+    # T = S = 1001: 8 key tiles with a 105-key tail, 251 query blocks with a 1-query tail.
+    prob = inputs.make("ragged", T=1001, S=1001, pos_offset=0, seed=11, dtype=dtype)
+    stats, _, _ = run_full(prob, _ix(prob, bf16_ix, fp8_ix))
+    assert stats["rows"] == 1001
+
+
+def test_tiny_1k_workload(bf16_ix):
+    prob = inputs.workload("tiny_1k")
+    stats, gi, _ = run_full(prob, bf16_ix)
+    # Rows with at most 512 visible keys keep all of them.
+    for t in range(512):
+        assert sorted(gi[t, :t + 1].tolist()) == list(range(t + 1))
+
+
+@pytest.mark.parametrize("dtype", [inputs.BF16, inputs.FP8_E4M3])
+def test_pos_offset_chunk(dtype, bf16_ix, fp8_ix):
+    # A 300-token chunk at position 1700 of a 2000-key cache (chunked prefill).
+    prob = inputs.make("chunk", T=300, S=2000, pos_offset=1700, seed=12, dtype=dtype)
+    run_full(prob, _ix(prob, bf16_ix, fp8_ix))
+
+
+@pytest.mark.parametrize("pos", [506, 507, 508, 509])
+def test_visible_count_around_512(pos, bf16_ix):
+    # Rows see 507..516 keys: fewer than, exactly and just over 512.
+    prob = inputs.make("edge512", T=7, S=700, pos_offset=pos, seed=13, dtype=inputs.BF16)
+    stats, gi, _ = run_full(prob, bf16_ix)
+    for t in range(7):
+        n = prob.n_visible(t)
+        if n <= 512:
+            assert sorted(gi[t, :n].tolist()) == list(range(n))
+
+
+def test_single_query_split_merge(bf16_ix, fp8_ix):
+    # T = 1 takes the one-query kernel with the key range split over many CTAs + merge kernel.
+    for dtype, ix in ((inputs.BF16, bf16_ix), (inputs.FP8_E4M3, fp8_ix)):
+        prob = inputs.make("decode1", T=1, S=9000, pos_offset=8999, seed=14, dtype=dtype)
+        run_full(prob, ix)
+
+
+def test_batched_decode_small(fp8_ix):
+    probs = [inputs.make(f"b{b}", T=1, S=6000, pos_offset=p, seed=20 + b,
+                         dtype=inputs.FP8_E4M3)
+             for b, p in enumerate((5999, 3000, 10, 511))]
+    q = torch.stack([p.q for p in probs]).cuda()
+    w = torch.stack([p.w for p in probs]).cuda()
+    k = torch.stack([p.k for p in probs]).cuda()
+    ks = torch.stack([p.kscale for p in probs]).cuda()
+    idx, sc = fp8_ix.score_topk_batched(q, w, k, ks, [p.pos_offset for p in probs])
+    fp8_ix.sync_status()
+    for b, prob in enumerate(probs):
+        parity.check_rows(prob, [0], idx[b].cpu().numpy(), sc[b].cpu().numpy())
+
+
+def test_batched_chunk_bf16(bf16_ix):
+    probs = [inputs.make(f"c{b}", T=37, S=3000, pos_offset=p, seed=30 + b, dtype=inputs.BF16)
+             for b, p in enumerate((2963, 100, 0))]
+    q = torch.stack([p.q for p in probs]).cuda()
+    w = torch.stack([p.w for p in probs]).cuda()
+    k = torch.stack([p.k for p in probs]).cuda()
+    idx, sc = bf16_ix.score_topk_batched(q, w, k, None, [p.pos_offset for p in probs])
+    bf16_ix.sync_status()
+    for b, prob in enumerate(probs):
+        parity.check_rows(prob, list(range(37)), idx[b].cpu().numpy(), sc[b].cpu().numpy())
+
+
+def test_tie_storm_lowest_indices(bf16_ix):
+    # k = 0: every score is exactly 0, so each row must return its lowest min(512, n) keys.
+    prob = inputs.make("ties", T=64, S=2000, pos_offset=1000, seed=15, dtype=inputs.BF16)
+    prob.k.zero_()
+    stats, gi, gs = run_full(prob, bf16_ix)
+    for t in range(64):
+        assert gi[t].tolist() == list(range(512))
+        assert np.all(gs[t] == 0.0)
+
+
+def test_all_negative_scores(bf16_ix):
+    prob = inputs.make("neg", T=50, S=1500, pos_offset=1400, seed=16, dtype=inputs.BF16)
+    prob.w.copy_(-prob.w.abs())
+    stats, _, gs = run_full(prob, bf16_ix)
+    assert np.all(gs[np.isfinite(gs)] <= 0.0)
+
+
+def test_zero_key_scales(fp8_ix):
+    prob = inputs.make("kscale0", T=40, S=1200, pos_offset=1100, seed=17, dtype=inputs.FP8_E4M3)
+    prob.kscale[::3] = 0.0
+    run_full(prob, fp8_ix)
+
+
+def test_deterministic(bf16_ix):
+    prob = inputs.make("det", T=257, S=3000, pos_offset=2743, seed=18, dtype=inputs.BF16)
+    dev = parity.to_device(prob)
+    a = [t.clone() for t in bf16_ix.score_topk(*dev, pos_offset=prob.pos_offset)]
+    b = bf16_ix.score_topk(*dev, pos_offset=prob.pos_offset)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0])
+    assert torch.equal(a[1].view(torch.int32), b[1].view(torch.int32))
+
+
+def test_invalid_arguments_rejected(bf16_ix, fp8_ix):
+    lib = ds4idx.load()
+    prob = inputs.make("args", T=8, S=64, pos_offset=0, seed=19, dtype=inputs.BF16)
+    q, w, k, _ = parity.to_device(prob)
+    oi = torch.empty((8, 512), dtype=torch.int32, device="cuda")
+    os_ = torch.empty((8, 512), dtype=torch.float32, device="cuda")
+    h = bf16_ix.handle
+    P = lambda t: t.data_ptr()  # noqa: E731
+    s = torch.cuda.current_stream().cuda_stream
+    ok = lib.ds4idx_score_topk(h, P(q), P(w), P(k), None, 8, 64, 0, 512, P(oi), P(os_), s)
+    assert ok == ds4idx.OK
+    cases = [
+        (None, P(w), P(k), None, 8, 64, 0, 512),            # null q
+        (P(q) + 2, P(w), P(k), None, 8, 64, 0, 512),        # misaligned q
+        (P(q), P(w), P(k), P(w), 8, 64, 0, 512),            # kscale given for bf16
+        (P(q), P(w), P(k), None, 8, 64, 0, 256),            # topk mismatch
+        (P(q), P(w), P(k), None, 8, 0, 0, 512),             # S = 0
+        (P(q), P(w), P(k), None, 8, 64, -1, 512),           # negative position
+        (P(q), P(w), P(k), None, 20000, 64, 0, 512),        # T > max_T
+        (P(q), P(w), P(k), None, 8, 1 << 20, 0, 512),       # S > max_S
+    ]
+    for c in cases:
+        st = lib.ds4idx_score_topk(h, *c, P(oi), P(os_), s)
+        assert st == ds4idx.ERR_INVALID_ARG, c
+    assert lib.ds4idx_score_topk(h, P(q), P(w), P(k), None, 8, 64, 0, 512, None, None, s) \
+        == ds4idx.ERR_INVALID_ARG
+    # FP8 handle without kscale
+    assert lib.ds4idx_score_topk(fp8_ix.handle, P(q), P(w), P(k), None, 8, 64, 0, 512, P(oi),
+                                 P(os_), s) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_score_topk(None, P(q), P(w), P(k), None, 8, 64, 0, 512, P(oi), P(os_),
+                                 s) == ds4idx.ERR_INVALID_ARG
+    # T = 0 is a no-op
+    assert lib.ds4idx_score_topk(h, P(q), P(w), P(k), None, 0, 64, 0, 512, P(oi), P(os_),
+                                 s) == ds4idx.OK
+    bf16_ix.sync_status()
+
+
+def test_unsupported_config():
+    with pytest.raises(ds4idx.Ds4IdxError) as e:
+        ds4idx.Indexer(ds4idx.BF16, max_T=16, max_S=16, n_heads=32)
+    assert e.value.status == ds4idx.ERR_UNSUPPORTED
