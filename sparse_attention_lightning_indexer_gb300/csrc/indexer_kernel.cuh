@@ -8,14 +8,15 @@
 //
 // One CTA owns NQ consecutive queries of one sequence (and, when the key range is split, one
 // slice of their keys). Its warps:
-//   warps 0..3   epilogue: warp w reads TMEM lanes 32w..32w+31, i.e. one key per thread, and
-//                reduces the 64 head columns of each query thread-locally (ReLU, * w, sum),
-//                so the T x S score matrix never leaves the SM;
-//   warp 4       TMA producer: Q block once, then 128-key K tiles into a ring of stages;
-//   warp 5       TMEM owner and MMA issuer: per key tile, D[128 keys, NQ*64 (query, head)]
+//   epilogue     4 or 8 warps; warp e reads TMEM lanes 32(e%4)..32(e%4)+31, i.e. one key per
+//                thread, for its group of queries, and reduces the 64 head columns of each
+//                query thread-locally (ReLU, * w, sum) with packed fp32x2 FMAs, so the T x S
+//                score matrix never leaves the SM; two warps per lane quadrant hide TMEM latency;
+//   TMA          Q block once, then 128-key K tiles into a ring of stages;
+//   MMA          TMEM owner and MMA issuer: per key tile, D[128 keys, NQ*64 (query, head)]
 //                = K_tile . Q_block^T on tcgen05 into one of two TMEM accumulators;
-//   warps 6..    one selector warp per query: filters the tile's scores against the running
-//                threshold, buffers survivors and merges them into its sorted Top-512 list.
+//   selectors    one warp per query: filters the tile's scores against the running threshold
+//                into an unsorted pool and radix-selects it back to exactly 512 when it fills.
 // Keys are the MMA M dimension (128 = all TMEM lanes) and (query, head) pairs the N dimension,
 // which is what makes the head reduction free of shuffles. The design on the page (a
 // threadgroup-tiled scorer, then a register-blocked K-resident scorer, then a streaming
@@ -33,7 +34,7 @@ constexpr int kHeads = 64;       // H_I
 constexpr int kDim = 128;        // d_I
 constexpr int kTopK = 512;
 constexpr int kTileKeys = 128;   // MMA M
-constexpr int kBufCap = 256;     // per-query candidate buffer
+constexpr int kPool = 1024;      // per-query candidate pool (the kept 512 + new candidates)
 constexpr int kScoreBufs = 4;    // depth of the epilogue -> selector score ring
 constexpr int kMaxBatch = 64;
 constexpr int kDtBf16 = 0;
@@ -63,7 +64,13 @@ struct KCfg {
   static constexpr int kKSteps = DT == kDtBf16 ? kDim / 16 : kDim / 32;
   static constexpr int kStepBytes = 32;                              // K bytes per MMA step
   static constexpr int kSelectors = DENSE ? 0 : NQ;
-  static constexpr int kWarps = 6 + kSelectors;
+  static constexpr int kEpiGroups = NQ >= 2 ? 2 : 1;        // warps per TMEM lane quadrant
+  static constexpr int kEpiWarps = 4 * kEpiGroups;
+  static constexpr int kQPerGroup = NQ / kEpiGroups;
+  static constexpr int kTmaWarp = kEpiWarps;
+  static constexpr int kMmaWarp = kEpiWarps + 1;
+  static constexpr int kSelWarp0 = kEpiWarps + 2;
+  static constexpr int kWarps = kEpiWarps + 2 + kSelectors;
   static constexpr int kThreads = 32 * kWarps;
   static constexpr uint32_t kTmemCols = 2 * kN <= 32 ? 32 : (2 * kN <= 64 ? 64 : (2 * kN <= 128 ? 128 : (2 * kN <= 256 ? 256 : 512)));
   static constexpr uint32_t kIdesc =
@@ -73,9 +80,9 @@ struct KCfg {
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKBytes;
   static constexpr int kOffScore = kOffW + NQ * kHeads * 4;
-  static constexpr int kOffList = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
-  static constexpr int kOffBuf = kOffList + (DENSE ? 0 : NQ * kTopK * 8);
-  static constexpr int kOffBar = kOffBuf + (DENSE ? 0 : NQ * kBufCap * 8);
+  static constexpr int kOffPool = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
+  static constexpr int kOffHist = kOffPool + (DENSE ? 0 : NQ * kPool * 8);
+  static constexpr int kOffBar = kOffHist + (DENSE ? 0 : NQ * 256 * 4);
   static constexpr int kNumBars = 2 * kStages + 4 + 2 * kScoreBufs + 1;
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
@@ -95,8 +102,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint8_t* sK = smem + C::kOffK;
   float* sW = reinterpret_cast<float*>(smem + C::kOffW);
   float* sScore = reinterpret_cast<float*>(smem + C::kOffScore);
-  uint64_t* sList = reinterpret_cast<uint64_t*>(smem + C::kOffList);
-  uint64_t* sBuf = reinterpret_cast<uint64_t*>(smem + C::kOffBuf);
+  uint64_t* sPool = reinterpret_cast<uint64_t*>(smem + C::kOffPool);
+  uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full = bars;                         // [kStages]  TMA -> MMA
   uint64_t* empty = full + C::kStages;           // [kStages]  MMA -> TMA
@@ -142,21 +149,21 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);
+      mbar_init(&tempty[i], C::kEpiWarps);
     }
     for (int i = 0; i < kScoreBufs; ++i) {
-      mbar_init(&sfull[i], 4);
+      mbar_init(&sfull[i], C::kEpiWarps);
       mbar_init(&sempty[i], NQ);
     }
     mbar_init(qfull, 1);
     *s_abort = 0u;
     fence_mbar_init();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == C::kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_k);
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == 4) {
+  if (warp == C::kTmaWarp) {
     // ================= TMA producer
     if (lane == 0 && n_tiles > 0) {
       mbar_arrive_expect_tx(qfull, C::kQBytes);
@@ -195,7 +202,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, s_abort, p.err);
       mbar_wait(qfull, 0, s_abort, p.err);
     }
-  } else if (warp == 5) {
+  } else if (warp == C::kMmaWarp) {
     // ================= MMA issuer (one thread)
     if (lane == 0 && n_tiles > 0) {
       int it = 0;
@@ -233,15 +240,17 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < 4) {
+  } else if (warp < C::kEpiWarps) {
     // ================= epilogue: TMEM -> ReLU . w -> per-key score
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int quad = warp & 3;
+    const int q0 = (warp >> 2) * C::kQPerGroup;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     for (int it = 0; it < n_tiles; ++it) {
       const int acc = it & 1;
       const uint32_t aph = (it >> 1) & 1;
       const int sb = it % kScoreBufs;
       const uint32_t sph = (it / kScoreBufs) & 1;
-      const int64_t key = static_cast<int64_t>(tile_lo + it) * kTileKeys + warp * 32 + lane;
+      const int64_t key = static_cast<int64_t>(tile_lo + it) * kTileKeys + quad * 32 + lane;
       float ks = 1.f;
       if (DT == kDtFp8) ks = key < p.S ? p.kscale[static_cast<int64_t>(b) * p.S + key] : 0.f;
       if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
@@ -250,30 +259,29 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         if (!mbar_wait_warp(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
       }
 #pragma unroll 1
-      for (int q = 0; q < NQ; ++q) {
+      for (int q = q0; q < q0 + C::kQPerGroup; ++q) {
         uint32_t r0[32], r1[32];
         const uint32_t col = tmem + lane_base + static_cast<uint32_t>(acc * C::kN + q * kHeads);
         tmem_ld32(col, r0);
         tmem_ld32(col + 32, r1);
         tmem_wait_ld();
+        // Four accumulator chains (heads = 0, 1, 2, 3 mod 4), two per packed fp32x2 FMA.
         const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        uint64_t acc01 = 0ull, acc23 = 0ull;
 #pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
+        for (int h4 = 0; h4 < 16; ++h4) {
           const float4 wv = w4[h4];
-          a0 = fmaf(wv.x, fmaxf(__uint_as_float(r0[4 * h4 + 0]), 0.f), a0);
-          a1 = fmaf(wv.y, fmaxf(__uint_as_float(r0[4 * h4 + 1]), 0.f), a1);
-          a2 = fmaf(wv.z, fmaxf(__uint_as_float(r0[4 * h4 + 2]), 0.f), a2);
-          a3 = fmaf(wv.w, fmaxf(__uint_as_float(r0[4 * h4 + 3]), 0.f), a3);
+          const uint32_t* r = h4 < 8 ? r0 + 4 * h4 : r1 + 4 * (h4 - 8);
+          const float x0 = fmaxf(__uint_as_float(r[0]), 0.f);
+          const float x1 = fmaxf(__uint_as_float(r[1]), 0.f);
+          const float x2 = fmaxf(__uint_as_float(r[2]), 0.f);
+          const float x3 = fmaxf(__uint_as_float(r[3]), 0.f);
+          acc01 = fma_f32x2(pack_f32x2(x0, x1), pack_f32x2(wv.x, wv.y), acc01);
+          acc23 = fma_f32x2(pack_f32x2(x2, x3), pack_f32x2(wv.z, wv.w), acc23);
         }
-#pragma unroll
-        for (int h4 = 0; h4 < 8; ++h4) {
-          const float4 wv = w4[8 + h4];
-          a0 = fmaf(wv.x, fmaxf(__uint_as_float(r1[4 * h4 + 0]), 0.f), a0);
-          a1 = fmaf(wv.y, fmaxf(__uint_as_float(r1[4 * h4 + 1]), 0.f), a1);
-          a2 = fmaf(wv.z, fmaxf(__uint_as_float(r1[4 * h4 + 2]), 0.f), a2);
-          a3 = fmaf(wv.w, fmaxf(__uint_as_float(r1[4 * h4 + 3]), 0.f), a3);
-        }
+        float a0, a1, a2, a3;
+        unpack_f32x2(acc01, a0, a1);
+        unpack_f32x2(acc23, a2, a3);
         float score = (a0 + a1) + (a2 + a3);
         if (DT == kDtFp8) score *= ks;
         if (DENSE) {
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
             p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
           }
         } else {
-          sScore[(sb * NQ + q) * kTileKeys + warp * 32 + lane] = score;
+          sScore[(sb * NQ + q) * kTileKeys + quad * 32 + lane] = score;
         }
       }
       tc_fence_before();
@@ -295,18 +303,16 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     }
   } else if (!DENSE) {
     // ================= selector: one warp per query of the block
-    const int q = warp - 6;
-    uint64_t* list = sList + q * kTopK;
-    uint64_t* buf = sBuf + q * kBufCap;
-    for (int i = lane; i < kTopK; i += 32) list[i] = 0ull;
-    __syncwarp();
+    const int q = warp - C::kSelWarp0;
+    uint64_t* pool = sPool + q * kPool;
+    uint32_t* hist = sHist + q * 256;
     const int64_t t = t0 + q;
     const bool valid = t < p.T;
     const int64_t pt = pos_b + t;
     const int64_t vis_end = valid ? (pt < p.S - 1 ? pt : p.S - 1) + 1 : 0;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    uint64_t theta = 0ull;
-    int nbuf = 0;
+    uint64_t theta = 0ull;  // exact 512th best word so far (0 until 512 words were seen)
+    int n = 0;              // words in the pool
     for (int it = 0; it < n_tiles; ++it) {
       const int sb = it % kScoreBufs;
       const uint32_t sph = (it / kScoreBufs) & 1;
@@ -320,29 +326,41 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                                          : 0ull;
         const bool pass = u > theta;
         const uint32_t m = __ballot_sync(0xffffffffu, pass);
-        if (pass) buf[nbuf + __popc(m & lt_mask)] = u;
-        nbuf += __popc(m);
+        if (pass) pool[n + __popc(m & lt_mask)] = u;
+        n += __popc(m);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      if (nbuf > kBufCap - kTileKeys) {
-        merge_buffer<kTopK, kBufCap>(list, buf, nbuf, lane);
-        theta = list[kTopK - 1];
-        nbuf = 0;
+      if (n > kPool - kTileKeys) {
+        theta = select_compact<kTopK>(pool, n, hist, lane);
+        n = kTopK;
       }
     }
-    if (nbuf > 0) merge_buffer<kTopK, kBufCap>(list, buf, nbuf, lane);
+    if (n > kTopK) n = (select_compact<kTopK>(pool, n, hist, lane), kTopK);
     __syncwarp();
+    // Final order: sort the (at most 512) survivors in registers, best first.
+    constexpr int R = kTopK / 32;
+    uint64_t v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int i = lane * R + r;
+      v[r] = i < n ? pool[i] : 0ull;
+    }
+    warp_sort_desc<R>(v, lane);
     if (valid && !*s_abort) {
       const int64_t row = static_cast<int64_t>(b) * p.T + t;
       if (p.n_splits > 1) {
-        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
-        for (int i = lane; i < kTopK; i += 32) dst[i] = list[i];
+        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK + lane * R;
+#pragma unroll
+        for (int r = 0; r < R; ++r) dst[r] = v[r];
       } else {
-        for (int i = lane; i < kTopK; i += 32) {
-          const uint64_t u = list[i];
-          p.out_idx[row * kTopK + i] = u ? key_index(u) : -1;
-          if (p.out_score) p.out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
+        int32_t* oi = p.out_idx + row * kTopK + lane * R;
+#pragma unroll
+        for (int r = 0; r < R; ++r) oi[r] = v[r] ? key_index(v[r]) : -1;
+        if (p.out_score) {
+          float* os = p.out_score + row * kTopK + lane * R;
+#pragma unroll
+          for (int r = 0; r < R; ++r) os[r] = v[r] ? key_score(v[r]) : -__int_as_float(0x7f800000);
         }
       }
     }
@@ -351,7 +369,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }

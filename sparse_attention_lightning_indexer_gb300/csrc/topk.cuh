@@ -8,11 +8,12 @@
 // (the Top-512 rule of "DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화", 섹션별 상세), with no
 // tie left open.
 //
-// The per-query state is a list of k words sorted descending plus an unsorted buffer of
-// candidates that beat the list's last word (the running threshold). When the buffer fills,
-// one warp sorts it and merges it into the list with bitonic networks in shared memory; the
-// threshold can only rise. The page replaced a bitonic sort plus merge cascade over all scores
-// with a streaming Top-512; here bitonic networks only ever see the small buffer.
+// Streaming selection per query (one warp): an unsorted pool holds every candidate that beat
+// the running threshold theta (the exact k-th best word seen so far, 0 before k words were
+// seen). When the pool nears capacity, an exact radix select finds the k-th largest word,
+// compacts the pool to exactly the k largest and raises theta to it. Only the final k words are
+// ever sorted, once, in registers. The page replaced a bitonic sort plus a merge cascade with a
+// streaming Top-512; here no sorting network ever runs on the stream itself.
 #pragma once
 #include <cstdint>
 
@@ -33,6 +34,121 @@ __device__ __forceinline__ int32_t key_index(uint64_t u) {
   return static_cast<int32_t>(~static_cast<uint32_t>(u));
 }
 
+__device__ __forceinline__ uint64_t umax64(uint64_t a, uint64_t b) { return a > b ? a : b; }
+__device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < b ? a : b; }
+
+// Exact radix select over pool[0..n), n > K: afterwards pool[0..K) holds exactly the K largest
+// words (unordered) and the K-th largest is returned. One warp; `hist` is 256 words of shared
+// scratch owned by this warp. Digits of 8 bits from the top; a digit pass stops as soon as the
+// bin holding the K-th word is kept whole, so typical score distributions need 2-4 passes and
+// only exact score ties ever reach the index bits.
+template <int K>
+__device__ __noinline__ uint64_t select_compact(uint64_t* pool, int n, uint32_t* hist, int lane) {
+  uint64_t prefix = 0ull;  // the digits fixed so far (bits above `shift`)
+  uint32_t need = K;       // rank of the K-th word among words matching `prefix`
+  int shift = 56;
+  for (;; shift -= 8) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
+    __syncwarp();
+    const uint64_t hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+    for (int i = lane; i < n; i += 32) {
+      const uint64_t u = pool[i];
+      if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & 255u], 1u);
+    }
+    __syncwarp();
+    // Lane l owns bins 8l..8l+7. above = number of matching words in higher bins.
+    uint32_t c[8];
+    uint32_t s = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      c[j] = hist[lane * 8 + j];
+      s += c[j];
+    }
+    uint32_t incl = s;  // inclusive suffix sum over lanes >= lane
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t v = __shfl_down_sync(0xffffffffu, incl, off);
+      if (lane + off < 32) incl += v;
+    }
+    uint32_t run = incl - s;
+    int bin = -1;
+    uint32_t bin_above = 0, bin_cnt = 0;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      if (bin < 0 && run < need && run + c[j] >= need) {
+        bin = lane * 8 + j;
+        bin_above = run;
+        bin_cnt = c[j];
+      }
+      run += c[j];
+    }
+    const uint32_t who = __ballot_sync(0xffffffffu, bin >= 0);
+    const int src = __ffs(who) - 1;
+    bin = __shfl_sync(0xffffffffu, bin, src);
+    bin_above = __shfl_sync(0xffffffffu, bin_above, src);
+    bin_cnt = __shfl_sync(0xffffffffu, bin_cnt, src);
+    prefix |= static_cast<uint64_t>(bin) << shift;
+    need -= bin_above;
+    if (bin_cnt == need || shift == 0) break;
+    __syncwarp();
+  }
+  // Keep exactly the words whose digits down to `shift` are >= the cut.
+  const uint64_t cut = prefix >> shift;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  int out = 0;
+  uint64_t mn = ~0ull;
+  for (int base = 0; base < n; base += 32) {
+    const int i = base + lane;
+    const uint64_t u = i < n ? pool[i] : 0ull;
+    const bool keep = i < n && (u >> shift) >= cut;
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    if (keep) {
+      pool[out + __popc(m & lt_mask)] = u;
+      mn = umin64(mn, u);
+    }
+    out += __popc(m);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mn = umin64(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+  __syncwarp();
+  return mn;
+}
+
+// Bitonic sort, descending, of 32*R words held in registers by one warp, element e = lane*R + r.
+// Distances below R are register swaps; larger ones exchange through shuffles.
+template <int R>
+__device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[R], int lane) {
+  constexpr int N = 32 * R;
+#pragma unroll
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      if (j >= R) {
+        const int lj = j / R;
+        const bool lower = (lane & lj) == 0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const uint64_t other = __shfl_xor_sync(0xffffffffu, v[r], lj);
+          const bool desc = ((lane * R + r) & k) == 0;
+          v[r] = (lower == desc) ? umax64(v[r], other) : umin64(v[r], other);
+        }
+      } else {
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          if ((r & j) == 0) {
+            const bool desc = ((lane * R + r) & k) == 0;
+            const uint64_t a = v[r], b = v[r | j];
+            const bool swap = desc ? (a < b) : (a > b);
+            v[r] = swap ? b : a;
+            v[r | j] = swap ? a : b;
+          }
+        }
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {
   const uint64_t a = x[i], b = x[l];
   if (a < b) {
@@ -41,7 +157,7 @@ __device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {
   }
 }
 
-// Sorts a bitonic sequence x[0..n) descending (one warp; n a power of two >= 64).
+// Sorts a bitonic sequence x[0..N) descending (one warp, shared memory).
 template <int N>
 __device__ __forceinline__ void bitonic_merge_desc(uint64_t* x, int lane) {
 #pragma unroll 1
@@ -55,71 +171,13 @@ __device__ __forceinline__ void bitonic_merge_desc(uint64_t* x, int lane) {
   }
 }
 
-// Full bitonic sort of x[0..N) descending (one warp).
-template <int N>
-__device__ __forceinline__ void bitonic_sort_desc(uint64_t* x, int lane) {
-#pragma unroll 1
-  for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll 1
-    for (int j = k >> 1; j > 0; j >>= 1) {
-#pragma unroll
-      for (int p = lane; p < N / 2; p += 32) {
-        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-        const int l = i + j;
-        const uint64_t a = x[i], b = x[l];
-        const bool desc = (i & k) == 0;
-        if (desc ? (a < b) : (a > b)) {
-          x[i] = b;
-          x[l] = a;
-        }
-      }
-      __syncwarp();
-    }
-  }
-}
-
-// x[0..N/2) and x[N/2..N) are each sorted descending; sorts x[0..N) descending.
-template <int N>
-__device__ __forceinline__ void merge_sorted_halves_desc(uint64_t* x, int lane) {
-#pragma unroll
-  for (int i = lane; i < N / 2; i += 32) cmp_swap_desc(x, i, N - 1 - i);
-  __syncwarp();
-  bitonic_merge_desc<N / 2>(x, lane);
-  bitonic_merge_desc<N / 2>(x + N / 2, lane);
-}
-
-// list[0..K) sorted descending (0-padded); buf[0..n) unsorted candidates, capacity C <= K.
-// Afterwards list holds the K largest of list U buf, sorted descending. One warp.
-template <int K, int C>
-__device__ __forceinline__ void merge_buffer(uint64_t* list, uint64_t* buf, int n, int lane) {
-  static_assert(C <= K, "buffer larger than the list");
-  for (int i = n + lane; i < C; i += 32) buf[i] = 0ull;
-  __syncwarp();
-  bitonic_sort_desc<C>(buf, lane);
-  // At most C of the buffer can enter the top K, so list[0..K-C) stays; the top C of
-  // list[K-C..K) U buf is the elementwise max against the reversed buffer (a bitonic sequence).
-  uint64_t* tail = list + (K - C);
-#pragma unroll
-  for (int i = lane; i < C; i += 32) {
-    const uint64_t a = tail[i], b = buf[C - 1 - i];
-    tail[i] = a > b ? a : b;
-  }
-  __syncwarp();
-  bitonic_merge_desc<C>(tail, lane);
-  if (K == 2 * C) {
-    merge_sorted_halves_desc<K>(list, lane);
-  } else {
-    static_assert(K == 2 * C || K == C, "unsupported list/buffer ratio");
-  }
-}
-
 // a[0..K) and b[0..K) sorted descending; a becomes the K largest of a U b, sorted. One warp.
 template <int K>
 __device__ __forceinline__ void merge_lists(uint64_t* a, const uint64_t* b, int lane) {
 #pragma unroll
   for (int i = lane; i < K; i += 32) {
     const uint64_t x = a[i], y = b[K - 1 - i];
-    a[i] = x > y ? x : y;
+    a[i] = umax64(x, y);
   }
   __syncwarp();
   bitonic_merge_desc<K>(a, lane);
