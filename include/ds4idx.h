@@ -49,7 +49,9 @@ typedef enum {
   DS4IDX_ERR_ALLOC = -3,          /* workspace allocation failed at create */
   DS4IDX_ERR_LAUNCH = -4,         /* a kernel launch or an enqueue failed */
   DS4IDX_ERR_DEVICE_TIMEOUT = -5, /* a kernel gave up on a bounded device-side wait */
-  DS4IDX_ERR_CUDA = -6            /* another CUDA runtime or driver call failed */
+  DS4IDX_ERR_CUDA = -6,           /* another CUDA runtime or driver call failed */
+  DS4IDX_ERR_SCRATCH_LIMIT = -7   /* request needs more than the fixed scratch of the
+                                     no-allocation entry point */
 } ds4idx_status;
 
 typedef enum { DS4IDX_BF16 = 0, DS4IDX_FP8_E4M3 = 1 } ds4idx_dtype;
@@ -121,6 +123,38 @@ const char* ds4idx_status_string(int status);
 
 /* Library ABI version: (major << 16) | minor. */
 int ds4idx_version(void);
+
+/* No-allocation variant of ds4idx_score_topk_batched. The pages have no counterpart: this is an
+ * integration aid for callers that cannot allocate device memory when they call the indexer.
+ * Examples are a serving engine that reserved all free HBM for its own KV-cache pool at start-up,
+ * and a host framework whose allocator must account for every device byte. Neither can let a
+ * library call cudaMalloc behind its back, and it may not be able to hold a ds4idx handle
+ * either, since a handle allocates its workspace at create.
+ *
+ * This entry point takes no handle and allocates nothing (no cudaMalloc, no cudaFree, no
+ * allocating library call). Its scratch, the per-split candidate lists of short sequences plus
+ * an error word, lives in one fixed 16 MiB array compiled into the library as file-scope
+ * __device__ storage. Every GPU that loads the library holds that array until the process exits.
+ *  - dtype is a ds4idx_dtype. All other arguments, layouts and rules are those of
+ *    ds4idx_score_topk_batched, with 1 <= B <= 64, 0 <= T, 1 <= S < 2^31 and topk = 512.
+ *  - Limit: a call whose key-range split needs more than 2^21 list words (B * T * splits * 512)
+ *    returns DS4IDX_ERR_SCRATCH_LIMIT and enqueues nothing. Only short sequences are split
+ *    (decode, chunks of a few tokens), and their plans stay well below the limit. Long prefills
+ *    are not split and use no scratch.
+ *  - Set-up: the first call on each device looks up the array's device address and sets kernel
+ *    attributes, with that device current. Make that first call before any stream capture.
+ *  - Sharing: all calls use the same array, and it keeps the previous call's contents. The error
+ *    word is cleared on `stream` at the start of every call; the candidate lists are always fully
+ *    written before they are read. Calls that can overlap on the GPU (different streams or host
+ *    threads without ordering between them) race on the array and corrupt each other's outputs,
+ *    so order them, for example on one stream.
+ *  - A kernel that gives up on a bounded device wait records it in the array's error word. This
+ *    entry point cannot report it; callers that need that status use a handle and
+ *    ds4idx_sync_status. */
+int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const void* q, const float* w,
+                                      const void* kcache, const float* kscale, int64_t T,
+                                      int64_t S, const int64_t* pos_offsets, int32_t topk,
+                                      int32_t* out_idx, float* out_score, void* stream);
 
 #ifdef __cplusplus
 }

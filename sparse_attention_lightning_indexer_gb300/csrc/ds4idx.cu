@@ -224,6 +224,7 @@ const char* ds4idx_status_string(int status) {
     case DS4IDX_ERR_LAUNCH: return "kernel launch failed";
     case DS4IDX_ERR_DEVICE_TIMEOUT: return "a kernel gave up on a bounded device wait";
     case DS4IDX_ERR_CUDA: return "CUDA runtime or driver error";
+    case DS4IDX_ERR_SCRATCH_LIMIT: return "request exceeds the fixed scratch of the no-allocation entry point";
     default: return "unknown status";
   }
 }
@@ -338,3 +339,106 @@ int ds4idx_destroy(ds4idx_t h) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation entry point
+// For callers that cannot allocate device memory at call time (an engine that pre-reserved its
+// HBM, an allocator that must account for every byte): the split-plan scratch lives in a fixed
+// array compiled into the library instead of a handle's workspace. See the header for the rules.
+namespace {
+
+constexpr size_t kNoAllocListWords = static_cast<size_t>(1) << 21;  // 16 MiB of list words
+
+// [0, kNoAllocListWords): per-split candidate lists; then the error word (own 256-byte line).
+static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocListWords + 32];
+
+struct NoAllocDevice {
+  std::once_flag once;
+  int status = DS4IDX_OK;
+  uint64_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int num_sms = 0;
+};
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// One-time set-up per device, run with that device current.
+int noalloc_setup(int dev) {
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  std::call_once(d.once, [&d, dev] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      d.status = DS4IDX_ERR_CUDA;
+      return;
+    }
+    if (!(major == 10 && minor == 3)) {
+      d.status = DS4IDX_ERR_UNSUPPORTED;
+      return;
+    }
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+      d.status = DS4IDX_ERR_CUDA;
+      return;
+    }
+    if (!load_encode() || set_smem_attr<kDtBf16, 4, false>() != cudaSuccess ||
+        set_smem_attr<kDtBf16, 1, false>() != cudaSuccess ||
+        set_smem_attr<kDtFp8, 4, false>() != cudaSuccess ||
+        set_smem_attr<kDtFp8, 1, false>() != cudaSuccess) {
+      d.status = DS4IDX_ERR_CUDA;
+      return;
+    }
+    d.scratch = static_cast<uint64_t*>(ptr);
+    d.num_sms = sms;
+    d.status = DS4IDX_OK;
+  });
+  return d.status;
+}
+
+}  // namespace
+
+extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const void* q,
+                                                 const float* w, const void* kcache,
+                                                 const float* kscale, int64_t T, int64_t S,
+                                                 const int64_t* pos_offsets, int32_t topk,
+                                                 int32_t* out_idx, float* out_score,
+                                                 void* stream) {
+  if (dtype != DS4IDX_BF16 && dtype != DS4IDX_FP8_E4M3) return DS4IDX_ERR_INVALID_ARG;
+  if (B < 1 || B > kMaxBatch || T < 0 || S < 1 || S > (1LL << 31) - 1 || !pos_offsets)
+    return DS4IDX_ERR_INVALID_ARG;
+  if (topk != kTopK) return DS4IDX_ERR_INVALID_ARG;
+  if (T == 0) return DS4IDX_OK;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return DS4IDX_ERR_CUDA;
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return DS4IDX_ERR_UNSUPPORTED;
+  const int st = noalloc_setup(dev);
+  if (st != DS4IDX_OK) return st;
+  const NoAllocDevice& d = g_noalloc_dev[dev];
+
+  int64_t max_vis = 0;
+  for (int b = 0; b < B; ++b) {
+    if (pos_offsets[b] < 0 || pos_offsets[b] > (1LL << 40)) return DS4IDX_ERR_INVALID_ARG;
+    max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
+  }
+  if (plan_partial_words(make_plan(d.num_sms, B, T, max_vis), B, T) > kNoAllocListWords)
+    return DS4IDX_ERR_SCRATCH_LIMIT;
+
+  // A stack handle that borrows the fixed scratch; the shared launch path does the rest.
+  ds4idx_handle h;
+  h.cfg.n_heads = kHeads;
+  h.cfg.head_dim = kDim;
+  h.cfg.topk = kTopK;
+  h.cfg.dtype = dtype;
+  h.cfg.max_T = T;
+  h.cfg.max_S = S;
+  h.cfg.max_batch = kMaxBatch;
+  h.device = dev;
+  h.num_sms = d.num_sms;
+  h.partial = d.scratch;
+  h.partial_words = kNoAllocListWords;
+  h.err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords);
+  if (cudaMemsetAsync(h.err, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DS4IDX_ERR_LAUNCH;
+  return run(&h, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score, nullptr,
+             stream);
+}

@@ -28,10 +28,11 @@ ERR_ALLOC = -3
 ERR_LAUNCH = -4
 ERR_DEVICE_TIMEOUT = -5
 ERR_CUDA = -6
+ERR_SCRATCH_LIMIT = -7
 
 EXPORTS = ("ds4idx_create", "ds4idx_score_topk", "ds4idx_score_topk_batched",
            "ds4idx_score_dense_debug", "ds4idx_sync_status", "ds4idx_destroy",
-           "ds4idx_status_string", "ds4idx_version")
+           "ds4idx_status_string", "ds4idx_version", "ds4idx_score_topk_batched_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -82,6 +83,9 @@ def load(path: str | None = None):
         lib.ds4idx_status_string.restype = ctypes.c_char_p
         lib.ds4idx_version.argtypes = []
         lib.ds4idx_version.restype = ctypes.c_int
+        lib.ds4idx_score_topk_batched_noalloc.argtypes = [i32, i32, vp, vp, vp, vp, i64, i64, vp,
+                                                          i32, vp, vp, vp]
+        lib.ds4idx_score_topk_batched_noalloc.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
