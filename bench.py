@@ -146,9 +146,56 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def cpu_baseline(prob, budget_s=10.0, seed=0):
-    """Times the fp64 oracle on a bounded, evenly spread row sample of `prob`."""
+def aggregate(local_ms, units_per_rank, device=None):
+    """Whole-job throughput across ranks: the slowest rank's time bounds the job.
+
+    Returns (max_ms, units/s over all ranks). With one process this is local_ms and
+    units_per_rank / time. Collective use: one MAX all-reduce of a scalar (timing only).
+    """
+    world = 1
+    t_max = float(local_ms)
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        world = torch.distributed.get_world_size()
+        tt = torch.tensor([float(local_ms)], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        t_max = float(tt.item())
+    return t_max, world * units_per_rank / (t_max / 1000.0)
+
+
+DECODE = "decode_8x262144"
+JOBS = sorted(inputs.WORKLOADS) + [DECODE]
+
+
+def load_job(name):
+    """(problems, batched): one problem, or the 8 independent decode sequences."""
+    if name == DECODE:
+        return inputs.decode_batch(**{k: v for k, v in inputs.DECODE_BATCH.items()}), True
+    return [inputs.workload(name)], False
+
+
+def count_launches(step):
+    """Kernel launches of one step, counted by the CUDA profiler (not assumed)."""
+    from torch.profiler import ProfilerActivity, profile
+    with profile(activities=[ProfilerActivity.CUDA]) as prof:
+        step()
+        torch.cuda.synchronize()
+    names = [e.name for e in prof.events() if e.device_type.name == "CUDA"]
+    return sum(1 for n in names if "indexer_kernel" in n or "merge_splits_kernel" in n)
+
+
+def cpu_baseline(probs, budget_s=10.0):
+    """Times the fp64 oracle on a bounded row sample of the workload (all host threads)."""
     from oracle import oracle as orc
+    if len(probs) > 1:  # independent decode sequences: one row each
+        t0 = time.perf_counter()
+        for p in probs:
+            q, k = p.codes()
+            orc.topk(p.dtype, q, p.w.numpy(), k, p.kscale.numpy(), p.pos_offset, p.topk)
+        dt = time.perf_counter() - t0
+        return {"value": len(probs) / dt, "unit": UNIT, "cores": orc.num_threads(),
+                "kind": "oracle",
+                "sample": f"all {len(probs)} decode queries ({probs[0].S} keys each), {dt:.1f} s"}
+    prob = probs[0]
     q, k = prob.codes()
     ks = None if prob.kscale is None else prob.kscale.numpy()
     w = prob.w.numpy()
@@ -173,7 +220,8 @@ def run_reference(args, rank, world):
     """Reference arm: the fp64 CPU oracle, timed on this host's cores (rank 0 only)."""
     if rank != 0:
         return
-    prob = inputs.workload(args.workload)
+    probs, _ = load_job(args.workload)
+    prob = probs[0]
     from oracle import oracle as orc
     q, k = prob.codes()
     ks = None if prob.kscale is None else prob.kscale.numpy()
@@ -197,10 +245,12 @@ def run_reference(args, rank, world):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * total / args.steps,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic",
-           "config": {"workload": prob.name, "T": prob.T, "S": prob.S, "H_I": inputs.H_I,
-                      "d_I": inputs.D_I, "topk": prob.topk, "pos_offset": prob.pos_offset},
+           "config": {"workload": args.workload, "B": len(probs), "T": prob.T, "S": prob.S,
+                      "H_I": inputs.H_I, "d_I": inputs.D_I, "topk": prob.topk,
+                      "pos_offset": prob.pos_offset, "seed": prob.meta.get("seed")},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                            "sample": f"{per_step} random query rows per step of {prob.name}"},
+                            "sample": f"{per_step} random query rows per step of {prob.name} "
+                                      f"(full causal rows, fp64 scores + full sort)"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
@@ -219,24 +269,39 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.barrier()
     ds4idx.load()
 
-    prob = inputs.workload(args.workload)
+    probs, batched = load_job(args.workload)
+    prob = probs[0]
+    B = len(probs)
     dev = torch.device("cuda", local_rank)
-    log(f"[rank {rank}] workload {prob.name}: T={prob.T} S={prob.S} dtype={prob.dtype}")
-    q = prob.q.to(dev)
-    w = prob.w.to(dev)
-    k = prob.k.to(dev)
-    ks = None if prob.kscale is None else prob.kscale.to(dev)
-    ix = ds4idx.Indexer(prob.dtype, max_T=prob.T, max_S=prob.S)
+    log(f"[rank {rank}] workload {args.workload}: B={B} T={prob.T} S={prob.S} dtype={prob.dtype}")
+
+    def stacked(attr):
+        ts = [getattr(p, attr) for p in probs]
+        if ts[0] is None:
+            return None
+        return torch.stack(ts) if batched else ts[0]
+
+    host = {a: stacked(a) for a in ("q", "w", "k", "kscale")}
+    q, w, k = (host[a].to(dev) for a in ("q", "w", "k"))
+    ks = None if host["kscale"] is None else host["kscale"].to(dev)
+    ix = ds4idx.Indexer(prob.dtype, max_T=prob.T, max_S=prob.S, max_batch=B)
     stream = torch.cuda.current_stream()
-    out_idx = torch.empty((prob.T, prob.topk), dtype=torch.int32, device=dev)
-    out_sc = torch.empty((prob.T, prob.topk), dtype=torch.float32, device=dev)
+    out_shape = (B, prob.T, prob.topk) if batched else (prob.T, prob.topk)
+    out_idx = torch.empty(out_shape, dtype=torch.int32, device=dev)
+    out_sc = torch.empty(out_shape, dtype=torch.float32, device=dev)
+    positions = [p.pos_offset for p in probs]
+    units_per_step = B * prob.T
 
     def step():
-        ix.score_topk(q, w, k, ks, prob.pos_offset, out_idx, out_sc, stream=stream)
+        if batched:
+            ix.score_topk_batched(q, w, k, ks, positions, out_idx, out_sc, stream=stream)
+        else:
+            ix.score_topk(q, w, k, ks, prob.pos_offset, out_idx, out_sc, stream=stream)
 
     for _ in range(args.warmup):
         step()
     ix.sync_status()
+    launches_per_step = count_launches(step)
 
     # ---- device-resident timing: K steps between two events, barrier + sync on both sides
     per_launch = []
@@ -259,21 +324,14 @@ def run_ours(args, rank, world, local_rank):
         total_ms = ev0.elapsed_time(ev1)
         per_launch = [marks[i].elapsed_time(marks[i + 1]) for i in range(args.steps)]
     ix.sync_status()
-    t_max = total_ms
-    if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max, value = aggregate(total_ms, units_per_step * args.steps, device=dev)
     ms_per_step = t_max / args.steps
-    value = world * prob.T * args.steps / (t_max / 1000.0)
 
     # ---- end to end through the C ABI with pinned host buffers
-    hq = prob.q.pin_memory()
-    hw = prob.w.pin_memory()
-    hk = prob.k.pin_memory()
-    hks = None if prob.kscale is None else prob.kscale.pin_memory()
-    ho_idx = torch.empty((prob.T, prob.topk), dtype=torch.int32).pin_memory()
-    ho_sc = torch.empty((prob.T, prob.topk), dtype=torch.float32).pin_memory()
+    hq, hw, hk = (host[a].pin_memory() for a in ("q", "w", "k"))
+    hks = None if host["kscale"] is None else host["kscale"].pin_memory()
+    ho_idx = torch.empty(out_shape, dtype=torch.int32).pin_memory()
+    ho_sc = torch.empty(out_shape, dtype=torch.float32).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hq, hw, hk) + ((hks,) if hks is not None else ()))
     d2h = ho_idx.numel() * 4 + ho_sc.numel() * 4
 
@@ -283,7 +341,7 @@ def run_ours(args, rank, world, local_rank):
         k.copy_(hk, non_blocking=True)
         if ks is not None:
             ks.copy_(hks, non_blocking=True)
-        ix.score_topk(q, w, k, ks, prob.pos_offset, out_idx, out_sc, stream=stream)
+        step()
         ho_idx.copy_(out_idx, non_blocking=True)
         ho_sc.copy_(out_sc, non_blocking=True)
 
@@ -299,25 +357,22 @@ def run_ours(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
     ix.sync_status()
-    e2e_value = world * prob.T * e2e_steps / (e2e_ms / 1000.0)
+    e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1), units_per_step * e2e_steps, device=dev)
 
     # ---- spot parity check of a few rows against the oracle (outside every timed region)
     spot = "skipped"
     if rank == 0:
         try:
-            sys.path.insert(0, os.path.join(ROOT, "tests"))
             from tests import parity
-            rows = [0, prob.T // 3, prob.T - 1]
-            gi = out_idx.cpu().numpy()[rows]
-            gs = out_sc.cpu().numpy()[rows]
-            parity.check_rows(prob, rows, gi, gs)
-            spot = f"{len(rows)} rows match the oracle"
+            gi_all, gs_all = out_idx.cpu().numpy(), out_sc.cpu().numpy()
+            checks = ([(b, [0]) for b in (0, B - 1)] if batched
+                      else [(0, [0, prob.T // 3, prob.T - 1])])
+            for b, rows in checks:
+                gi = gi_all[b][rows] if batched else gi_all[rows]
+                gs = gs_all[b][rows] if batched else gs_all[rows]
+                parity.check_rows(probs[b], rows, gi, gs)
+            spot = f"{sum(len(r) for _, r in checks)} rows match the oracle"
         except AssertionError as e:  # reported, never hidden
             spot = f"MISMATCH: {e}"
 
@@ -328,35 +383,49 @@ def run_ours(args, rank, world, local_rank):
         ix.close()
         return
 
-    flops, key_bytes, pairs = algorithmic(prob)
     peaks, peak_src = load_peaks()
-    avg_launch_ms = statistics.mean(per_launch)
-    launches_per_step = 1  # single sequence with T > 1 and enough query blocks: no split merge
+    avg_step_ms = statistics.mean(per_launch)
+    flops, key_bytes, pairs = algorithmic(prob)
+    flops *= B
+    key_bytes *= B
+    pairs *= B
     if prob.T == 1:
-        launches_per_step = 2
-    if prob.dtype == inputs.BF16:
-        peak = peaks["bf16_tflops"]
-        peak_note = f"bf16 dense, {peak_src} (burst)"
+        # decode: every visible key is read once from HBM per query; bytes bound the step
+        achieved = key_bytes / (avg_step_ms / 1000.0) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                    "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                    "traffic": traffic_for(args.workload),
+                    "peak_source": f"hbm copy bandwidth, {peak_src}",
+                    "algorithmic": f"{key_bytes:.4g} B = {B} x {prob.S} keys x 132 B "
+                                   f"(128 B E4M3 + 4 B scale)",
+                    "timed": "whole step: indexer kernel + split-merge kernel"}
     else:
-        peak = peaks["bf16_tflops"] * FP8_OVER_BF16
-        peak_note = f"fp8 dense = {peak_src} bf16 burst x {FP8_OVER_BF16} (nominal ratio)"
-    achieved = flops / (avg_launch_ms / 1000.0) / 1e12
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                "frac": achieved / peak, "traffic": traffic_for(prob.name),
-                "peak_source": peak_note,
-                "algorithmic": f"{flops:.4g} flop = 2*64*128 * {pairs:.4g} visible pairs",
-                "hbm_gbs_key_cache": key_bytes / (avg_launch_ms / 1000.0) / 1e9}
-    cpu = cpu_baseline(prob, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
+        if prob.dtype == inputs.BF16:
+            peak = peaks["bf16_tflops"]
+            peak_note = f"bf16 dense, {peak_src} (burst)"
+        else:
+            peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+            peak_note = f"fp8 dense = {peak_src} bf16 burst x {FP8_OVER_BF16} (nominal ratio)"
+        achieved = flops / (avg_step_ms / 1000.0) / 1e12
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                    "frac": achieved / peak, "traffic": traffic_for(args.workload),
+                    "peak_source": peak_note,
+                    "algorithmic": f"{flops:.4g} flop = 2*64*128 * {pairs:.4g} visible pairs",
+                    "timed": ("indexer kernel" if launches_per_step == 1
+                              else "whole step: indexer kernel + split-merge kernel")}
+    cpu = cpu_baseline(probs, budget_s=args.cpu_budget) if args.cpu_budget > 0 else None
     out = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
            "dtype": "bf16" if prob.dtype == inputs.BF16 else "fp8_e4m3",
            "data": "synthetic",
-           "config": {"workload": prob.name, "T": prob.T, "S": prob.S, "H_I": inputs.H_I,
-                      "d_I": inputs.D_I, "topk": prob.topk, "pos_offset": prob.pos_offset,
+           "config": {"workload": args.workload, "B": B, "T": prob.T, "S": prob.S,
+                      "H_I": inputs.H_I, "d_I": inputs.D_I, "topk": prob.topk,
+                      "pos_offset": positions if batched else prob.pos_offset,
                       "seed": prob.meta.get("seed"),
-                      "l2": "inputs larger than L2 (q is %.0f MiB)" % (
-                          prob.q.numel() * prob.q.element_size() / 2**20),
+                      "l2": "inputs larger than L2 (%s is %.0f MiB)" % (
+                          ("key cache", k.numel() * k.element_size() / 2**20) if prob.T == 1
+                          else ("q", q.numel() * q.element_size() / 2**20)),
                       "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
            "roofline": roofline,
            "cpu_baseline": cpu,
@@ -377,7 +446,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="prefill_64k", choices=sorted(inputs.WORKLOADS))
+    ap.add_argument("--workload", default="prefill_64k", choices=JOBS)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0 disables)")
