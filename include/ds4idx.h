@@ -124,6 +124,10 @@ const char* ds4idx_status_string(int status);
 /* Library ABI version: (major << 16) | minor. */
 int ds4idx_version(void);
 
+/* Number of kernels this library has enqueued in this process (all handles and entry points).
+ * Instrumentation for benchmarks: a successful compute call adds the launches it made. */
+uint64_t ds4idx_kernels_launched(void);
+
 /* No-allocation variant of ds4idx_score_topk_batched. The pages have no counterpart: this is an
  * integration aid for callers that cannot allocate device memory when they call the indexer.
  * Examples are a serving engine that reserved all free HBM for its own KV-cache pool at start-up,
@@ -144,8 +148,8 @@ int ds4idx_version(void);
  *  - Set-up: the first call on each device looks up the array's device address and sets kernel
  *    attributes, with that device current. Make that first call before any stream capture.
  *  - Sharing: all calls use the same array, and it keeps the previous call's contents. The error
- *    word is cleared on `stream` at the start of every call; the candidate lists are always fully
- *    written before they are read. Calls that can overlap on the GPU (different streams or host
+ *    word and the split tickets are cleared on `stream` at the start of every call; the candidate
+ *    lists are always fully written before they are read. Calls that can overlap on the GPU (different streams or host
  *    threads without ordering between them) race on the array and corrupt each other's outputs,
  *    so order them, for example on one stream.
  *  - A kernel that gives up on a bounded device wait records it in the array's error word. This

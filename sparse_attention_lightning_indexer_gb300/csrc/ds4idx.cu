@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -23,6 +24,8 @@ struct ds4idx_handle {
   uint32_t* err = nullptr;        // device error word
   uint64_t* partial = nullptr;    // per-split Top-512 lists
   size_t partial_words = 0;
+  uint32_t* counters = nullptr;   // per-block split tickets, zero between calls
+  size_t n_counters = 0;
 };
 
 namespace {
@@ -30,6 +33,8 @@ namespace {
 constexpr int kVersion = (1 << 16) | 0;
 constexpr int kMaxSplits = 64;
 constexpr int kMinTilesPerSplit = 4;
+
+std::atomic<uint64_t> g_launches{0};  // kernels this library has enqueued (process-wide)
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -67,12 +72,25 @@ Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
   pl.n_qb = static_cast<int>((T + pl.nq - 1) / pl.nq);
   const int64_t tiles = (max_vis + kTileKeys - 1) / kTileKeys;
   const int64_t blocks = B * pl.n_qb;
-  const int64_t target = 4LL * num_sms;
   int64_t splits = 1;
-  if (blocks < target) {
-    splits = (target + blocks - 1) / blocks;
-    splits = std::min<int64_t>(splits, kMaxSplits);
-    splits = std::min<int64_t>(splits, std::max<int64_t>(1, tiles / kMinTilesPerSplit));
+  if (blocks < 4LL * num_sms) {
+    // Few query blocks of similar size (decode, short chunks): split the key range so the CTAs
+    // fill whole waves of SMs. Every split repeats the Top-512 warm-up and adds a list to merge,
+    // so take the fewest splits whose wave occupancy is within 5% of the best achievable.
+    const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, tiles / kMinTilesPerSplit));
+    auto occupancy = [&](int64_t sp) {
+      const int64_t ctas = blocks * sp;
+      const int64_t waves = (ctas + num_sms - 1) / num_sms;
+      return static_cast<double>(ctas) / static_cast<double>(waves * num_sms);
+    };
+    double best = 0.0;
+    for (int64_t sp = 1; sp <= max_s; ++sp) best = std::max(best, occupancy(sp));
+    for (int64_t sp = 1; sp <= max_s; ++sp) {
+      if (occupancy(sp) >= best - 0.05) {
+        splits = sp;
+        break;
+      }
+    }
   }
   pl.tiles_per_split = static_cast<int>((tiles + splits - 1) / splits);
   pl.n_splits = static_cast<int>((tiles + pl.tiles_per_split - 1) / pl.tiles_per_split);
@@ -83,6 +101,9 @@ Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
 
 size_t plan_partial_words(const Plan& pl, int64_t B, int64_t T) {
   return pl.n_splits > 1 ? static_cast<size_t>(B * T) * pl.n_splits * kTopK : 0;
+}
+size_t plan_counters(const Plan& pl, int64_t B) {
+  return pl.n_splits > 1 ? static_cast<size_t>(B) * pl.n_qb : 0;
 }
 
 template <int DT, int NQ, bool DENSE>
@@ -116,7 +137,9 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const KParams& 
   using C = KCfg<DT, NQ, DENSE>;
   indexer_kernel<DT, NQ, DENSE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes,
                                   stream>>>(tq, tk, kp);
-  return cudaGetLastError();
+  const cudaError_t e = cudaGetLastError();
+  if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
+  return e;
 }
 
 template <int DT>
@@ -172,7 +195,8 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
     pl.tiles_per_split = static_cast<int>((S + kTileKeys - 1) / kTileKeys);
     pl.grid = pl.n_qb;
   }
-  if (plan_partial_words(pl, B, T) > h->partial_words) return DS4IDX_ERR_INVALID_ARG;
+  if (plan_partial_words(pl, B, T) > h->partial_words || plan_counters(pl, B) > h->n_counters)
+    return DS4IDX_ERR_INVALID_ARG;
 
   CUtensorMap tq, tk;
   if (!encode_rows(&tq, q, c.dtype, T * kHeads, B, kHeads * pl.nq)) return DS4IDX_ERR_INVALID_ARG;
@@ -185,6 +209,7 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
   kp.out_idx = out_idx;
   kp.out_score = out_score;
   kp.partial = h->partial;
+  kp.counters = h->counters;
   kp.dense = dense;
   kp.err = h->err;
   kp.T = T;
@@ -200,12 +225,6 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
                       ? launch_dt<kDtBf16>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream)
                       : launch_dt<kDtFp8>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream);
   if (e != cudaSuccess) return DS4IDX_ERR_LAUNCH;
-  if (!dense && pl.n_splits > 1) {
-    const int64_t rows = static_cast<int64_t>(B) * T;
-    merge_splits_kernel<<<static_cast<unsigned>((rows + 3) / 4), 128, 0, stream>>>(
-        h->partial, pl.n_splits, rows, out_idx, out_score);
-    if (cudaGetLastError() != cudaSuccess) return DS4IDX_ERR_LAUNCH;
-  }
   return DS4IDX_OK;
 }
 
@@ -214,6 +233,8 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
 extern "C" {
 
 int ds4idx_version(void) { return kVersion; }
+
+uint64_t ds4idx_kernels_launched(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* ds4idx_status_string(int status) {
   switch (status) {
@@ -264,25 +285,30 @@ int ds4idx_create(ds4idx_t* out, const ds4idx_config* cfg) {
   h->num_sms = prop.multiProcessorCount;
 
   // Workspace for the largest per-split candidate set any admissible call can need.
-  size_t words = 0;
+  size_t words = 0, counters = 0;
   for (int64_t B = 1; B <= cfg->max_batch; ++B) {
     const int64_t t_hi = std::min<int64_t>(cfg->max_T, 16LL * h->num_sms);
     for (int64_t T = 1; T <= t_hi; ++T) {
       const Plan pl = make_plan(h->num_sms, B, T, cfg->max_S);
       words = std::max(words, plan_partial_words(pl, B, T));
+      counters = std::max(counters, plan_counters(pl, B));
     }
   }
   h->partial_words = words;
-  if (cudaMalloc(&h->err, 16) != cudaSuccess) {
+  h->n_counters = counters;
+  // err word at [0], split tickets from [64] (own cache lines), all zeroed once here
+  const size_t misc_bytes = 256 + counters * sizeof(uint32_t);
+  if (cudaMalloc(&h->err, misc_bytes) != cudaSuccess) {
     delete h;
     return DS4IDX_ERR_ALLOC;
   }
+  h->counters = h->err + 64;
   if (words && cudaMalloc(&h->partial, words * sizeof(uint64_t)) != cudaSuccess) {
     cudaFree(h->err);
     delete h;
     return DS4IDX_ERR_ALLOC;
   }
-  if (cudaMemset(h->err, 0, 16) != cudaSuccess) {
+  if (cudaMemset(h->err, 0, misc_bytes) != cudaSuccess) {
     cudaFree(h->partial);
     cudaFree(h->err);
     delete h;
@@ -323,7 +349,8 @@ int ds4idx_sync_status(ds4idx_t h, void* stream) {
   if (cudaMemcpy(&word, h->err, sizeof word, cudaMemcpyDeviceToHost) != cudaSuccess)
     return DS4IDX_ERR_CUDA;
   if (word) {
-    cudaMemset(h->err, 0, sizeof word);
+    // A CTA that gave up may have left a split ticket half counted: start the next call clean.
+    cudaMemset(h->err, 0, 256 + h->n_counters * sizeof(uint32_t));
     return DS4IDX_ERR_DEVICE_TIMEOUT;
   }
   return DS4IDX_OK;
@@ -348,8 +375,11 @@ namespace {
 
 constexpr size_t kNoAllocListWords = static_cast<size_t>(1) << 21;  // 16 MiB of list words
 
-// [0, kNoAllocListWords): per-split candidate lists; then the error word (own 256-byte line).
-static __device__ __align__(256) uint64_t g_noalloc_scratch[kNoAllocListWords + 32];
+constexpr size_t kNoAllocTickets = 4096;  // split tickets, one per query block of a split plan
+// [0, kNoAllocListWords): per-split candidate lists; then the error word (own 256-byte line);
+// then the split tickets (32-bit, zeroed at every call together with the error word).
+static __device__ __align__(256) uint64_t
+    g_noalloc_scratch[kNoAllocListWords + 32 + kNoAllocTickets / 2];
 
 struct NoAllocDevice {
   std::once_flag once;
@@ -419,7 +449,8 @@ extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const
     if (pos_offsets[b] < 0 || pos_offsets[b] > (1LL << 40)) return DS4IDX_ERR_INVALID_ARG;
     max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
   }
-  if (plan_partial_words(make_plan(d.num_sms, B, T, max_vis), B, T) > kNoAllocListWords)
+  const Plan pl = make_plan(d.num_sms, B, T, max_vis);
+  if (plan_partial_words(pl, B, T) > kNoAllocListWords || plan_counters(pl, B) > kNoAllocTickets)
     return DS4IDX_ERR_SCRATCH_LIMIT;
 
   // A stack handle that borrows the fixed scratch; the shared launch path does the rest.
@@ -436,8 +467,11 @@ extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const
   h.partial = d.scratch;
   h.partial_words = kNoAllocListWords;
   h.err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords);
-  if (cudaMemsetAsync(h.err, 0, sizeof(uint32_t), static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  h.counters = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords + 32);
+  h.n_counters = kNoAllocTickets;
+  // The array keeps the previous call's contents: clear the error word and the tickets.
+  if (cudaMemsetAsync(h.err, 0, 256 + kNoAllocTickets * sizeof(uint32_t),
+                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return DS4IDX_ERR_LAUNCH;
   return run(&h, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score, nullptr,
              stream);

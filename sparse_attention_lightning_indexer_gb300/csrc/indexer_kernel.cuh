@@ -34,8 +34,6 @@ constexpr int kHeads = 64;       // H_I
 constexpr int kDim = 128;        // d_I
 constexpr int kTopK = 512;
 constexpr int kTileKeys = 128;   // MMA M
-constexpr int kPool = 1024;      // per-query candidate pool (the kept 512 + new candidates)
-constexpr int kScoreBufs = 4;    // depth of the epilogue -> selector score ring
 constexpr int kMaxBatch = 64;
 constexpr int kDtBf16 = 0;
 constexpr int kDtFp8 = 1;
@@ -46,6 +44,7 @@ struct KParams {
   int32_t* out_idx;      // [B, T, 512]
   float* out_score;      // [B, T, 512] or null
   uint64_t* partial;     // [B, T, n_splits, 512] packed lists when n_splits > 1
+  uint32_t* counters;    // [B * n_qb] split tickets (zero between calls) when n_splits > 1
   float* dense;          // [T, S] scores (debug variant)
   uint32_t* err;         // device error word
   int64_t T, S;
@@ -60,9 +59,18 @@ struct KCfg {
   static constexpr int kN = kHeads * NQ;                             // MMA N
   static constexpr int kQBytes = kN * kRowBytes;
   static constexpr int kKBytes = kTileKeys * kRowBytes;
-  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 6) : (NQ == 4 ? 6 : 8);
+  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 5) : (NQ == 4 ? 6 : 8);
   static constexpr int kKSteps = DT == kDtBf16 ? kDim / 16 : kDim / 32;
   static constexpr int kStepBytes = 32;                              // K bytes per MMA step
+  // Depth of the epilogue -> selector score ring: it lets selectors fall behind by that many
+  // tiles while they radix-select, without stalling the MMA pipeline.
+  static constexpr int kScoreBufs = NQ == 1 ? 16 : (DT == kDtFp8 ? 12 : 4);
+  // TMEM accumulators: all 512 columns, so a narrow (one-query) MMA can run up to 8 tiles
+  // ahead of the epilogue instead of waiting on a round trip per tile.
+  static constexpr int kAccBufs = 512 / kN;
+  // Per-query candidate pool (the kept 512 plus new candidates). One-query CTAs have the room
+  // for a pool that usually absorbs a whole key split without any intermediate select.
+  static constexpr int kPool = NQ == 1 ? 4096 : 1024;
   static constexpr int kSelectors = DENSE ? 0 : NQ;
   static constexpr int kEpiGroups = NQ >= 2 ? 2 : 1;        // warps per TMEM lane quadrant
   static constexpr int kEpiWarps = 4 * kEpiGroups;
@@ -72,7 +80,8 @@ struct KCfg {
   static constexpr int kSelWarp0 = kEpiWarps + 2;
   static constexpr int kWarps = kEpiWarps + 2 + kSelectors;
   static constexpr int kThreads = 32 * kWarps;
-  static constexpr uint32_t kTmemCols = 2 * kN <= 32 ? 32 : (2 * kN <= 64 ? 64 : (2 * kN <= 128 ? 128 : (2 * kN <= 256 ? 256 : 512)));
+  static constexpr uint32_t kTmemCols = 512;
+  static_assert(kAccBufs * kN == 512 && kAccBufs >= 2, "accumulators tile the TMEM columns");
   static constexpr uint32_t kIdesc =
       DT == kDtBf16 ? instr_desc(1u, 1u, kTileKeys, kN) : instr_desc(0u, 0u, kTileKeys, kN);
   // shared memory layout (offsets from a 1024-byte aligned base)
@@ -83,12 +92,84 @@ struct KCfg {
   static constexpr int kOffPool = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
   static constexpr int kOffHist = kOffPool + (DENSE ? 0 : NQ * kPool * 8);
   static constexpr int kOffBar = kOffHist + (DENSE ? 0 : NQ * 256 * 4);
-  static constexpr int kNumBars = 2 * kStages + 4 + 2 * kScoreBufs + 1;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
+  static_assert(kWarps * kTopK * 8 <= kStages * kKBytes, "merge slots reuse the K stages");
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
   static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
+
+template <int R>
+__device__ __forceinline__ void load_list(uint64_t (&v)[R], const uint64_t* src, int lane) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + lane * R);
+#pragma unroll
+  for (int i = 0; i < R / 2; ++i) {
+    const uint4 x = s4[i];
+    v[2 * i] = (static_cast<uint64_t>(x.y) << 32) | x.x;
+    v[2 * i + 1] = (static_cast<uint64_t>(x.w) << 32) | x.z;
+  }
+}
+template <int R>
+__device__ __forceinline__ void store_list(uint64_t* dst, const uint64_t (&v)[R], int lane) {
+  uint4* d4 = reinterpret_cast<uint4*>(dst + lane * R);
+#pragma unroll
+  for (int i = 0; i < R / 2; ++i)
+    d4[i] = make_uint4(static_cast<uint32_t>(v[2 * i]), static_cast<uint32_t>(v[2 * i] >> 32),
+                       static_cast<uint32_t>(v[2 * i + 1]),
+                       static_cast<uint32_t>(v[2 * i + 1] >> 32));
+}
+
+// Merges the n_splits sorted Top-512 lists of each query of a block into the final output. All
+// warps of the CTA take part: warp w folds lists w, w+W, ... into registers, then the W partial
+// results are combined pairwise in shared memory (`slots`, W x 512 words).
+template <class C>
+__device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* slots, int warp,
+                                  int lane) {
+  constexpr int R = kTopK / 32;
+  constexpr int W = C::kWarps;
+  const int used = p.n_splits < W ? p.n_splits : W;  // slots that receive lists
+  for (int q = 0; q < C::kN / kHeads; ++q) {
+    const int64_t t = t0 + q;
+    if (t >= p.T) break;
+    const int64_t row = static_cast<int64_t>(b) * p.T + t;
+    const uint64_t* lists = p.partial + row * p.n_splits * kTopK;
+    if (warp < used) {
+      uint64_t acc[R];
+      load_list<R>(acc, lists + warp * kTopK, lane);
+      for (int sp = warp + W; sp < p.n_splits; sp += W) {
+        uint64_t nxt[R];
+        load_list<R>(nxt, lists + sp * kTopK, lane);
+        warp_merge_desc<R>(acc, nxt, lane);
+      }
+      store_list<R>(slots + warp * kTopK, acc, lane);
+    }
+    __syncthreads();
+    for (int stride = 1; stride < used; stride *= 2) {
+      if (warp % (2 * stride) == 0 && warp + stride < used) {
+        uint64_t a[R], o[R];
+        load_list<R>(a, slots + warp * kTopK, lane);
+        load_list<R>(o, slots + (warp + stride) * kTopK, lane);
+        warp_merge_desc<R>(a, o, lane);
+        store_list<R>(slots + warp * kTopK, a, lane);
+      }
+      __syncthreads();
+    }
+    if (warp == 0) {
+      uint64_t v[R];
+      load_list<R>(v, slots, lane);
+      int32_t* oi = p.out_idx + row * kTopK + lane * R;
+#pragma unroll
+      for (int r = 0; r < R; ++r) oi[r] = v[r] ? key_index(v[r]) : -1;
+      if (p.out_score) {
+        float* os = p.out_score + row * kTopK + lane * R;
+#pragma unroll
+        for (int r = 0; r < R; ++r) os[r] = v[r] ? key_score(v[r]) : -__int_as_float(0x7f800000);
+      }
+    }
+    __syncthreads();
+  }
+}
 
 template <int DT, int NQ, bool DENSE>
 __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
@@ -107,13 +188,14 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
   uint64_t* full = bars;                         // [kStages]  TMA -> MMA
   uint64_t* empty = full + C::kStages;           // [kStages]  MMA -> TMA
-  uint64_t* tfull = empty + C::kStages;          // [2]        MMA -> epilogue
-  uint64_t* tempty = tfull + 2;                  // [2]        epilogue -> MMA
-  uint64_t* sfull = tempty + 2;                  // [kScoreBufs] epilogue -> selectors
-  uint64_t* sempty = sfull + kScoreBufs;         // [kScoreBufs] selectors -> epilogue
-  uint64_t* qfull = sempty + kScoreBufs;         // Q block landed
+  uint64_t* tfull = empty + C::kStages;          // [kAccBufs] MMA -> epilogue
+  uint64_t* tempty = tfull + C::kAccBufs;        // [kAccBufs] epilogue -> MMA
+  uint64_t* sfull = tempty + C::kAccBufs;        // [C::kScoreBufs] epilogue -> selectors
+  uint64_t* sempty = sfull + C::kScoreBufs;         // [C::kScoreBufs] selectors -> epilogue
+  uint64_t* qfull = sempty + C::kScoreBufs;         // Q block landed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
+  volatile uint32_t* s_last = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -147,11 +229,11 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], C::kEpiWarps);
     }
-    for (int i = 0; i < kScoreBufs; ++i) {
+    for (int i = 0; i < C::kScoreBufs; ++i) {
       mbar_init(&sfull[i], C::kEpiWarps);
       mbar_init(&sempty[i], NQ);
     }
@@ -210,8 +292,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       for (; ok && it < n_tiles; ++it) {
         const int st = it % C::kStages;
         const uint32_t sph = (it / C::kStages) & 1;
-        const int acc = it & 1;
-        const uint32_t aph = (it >> 1) & 1;
+        const int acc = it % C::kAccBufs;
+        const uint32_t aph = (it / C::kAccBufs) & 1;
         if (!mbar_wait(&full[st], sph, s_abort, p.err)) break;
         if (!mbar_wait(&tempty[acc], aph ^ 1u, s_abort, p.err)) break;
         tc_fence_after();
@@ -230,13 +312,13 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
             mma_fp8(d, a_desc, b_desc, C::kIdesc, ks > 0 ? 1u : 0u);
         }
         mma_commit(&empty[st]);
-        mma_commit(&tfull[it & 1]);
+        mma_commit(&tfull[acc]);
       }
       // Before TMEM is released every issued MMA must have completed: wait for the commit of
       // the last tile issued (the epilogue waits on the same phase).
       if (it > 0) {
         const int last = it - 1;
-        mbar_wait(&tfull[last & 1], (last >> 1) & 1, s_abort, p.err);
+        mbar_wait(&tfull[last % C::kAccBufs], (last / C::kAccBufs) & 1, s_abort, p.err);
       }
     }
     __syncwarp();
@@ -245,14 +327,30 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     const int quad = warp & 3;
     const int q0 = (warp >> 2) * C::kQPerGroup;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    // FP8 key scales are read two tiles ahead so their global-memory latency stays hidden
+    // (decode streams the cache once, so these reads miss in L2).
+    const float* kscale_b = DT == kDtFp8 ? p.kscale + static_cast<int64_t>(b) * p.S : nullptr;
+    auto load_scale = [&](int tile) -> float {
+      const int64_t k = static_cast<int64_t>(tile_lo + tile) * kTileKeys + quad * 32 + lane;
+      return (tile < n_tiles && k < p.S) ? __ldg(kscale_b + k) : 0.f;
+    };
+    float ks_next0 = 1.f, ks_next1 = 1.f;
+    if (DT == kDtFp8) {
+      ks_next0 = load_scale(0);
+      ks_next1 = load_scale(1);
+    }
     for (int it = 0; it < n_tiles; ++it) {
-      const int acc = it & 1;
-      const uint32_t aph = (it >> 1) & 1;
-      const int sb = it % kScoreBufs;
-      const uint32_t sph = (it / kScoreBufs) & 1;
+      const int acc = it % C::kAccBufs;
+      const uint32_t aph = (it / C::kAccBufs) & 1;
+      const int sb = it % C::kScoreBufs;
+      const uint32_t sph = (it / C::kScoreBufs) & 1;
       const int64_t key = static_cast<int64_t>(tile_lo + it) * kTileKeys + quad * 32 + lane;
       float ks = 1.f;
-      if (DT == kDtFp8) ks = key < p.S ? p.kscale[static_cast<int64_t>(b) * p.S + key] : 0.f;
+      if (DT == kDtFp8) {
+        ks = ks_next0;
+        ks_next0 = ks_next1;
+        ks_next1 = load_scale(it + 2);
+      }
       if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
       tc_fence_after();
       if (!DENSE) {
@@ -304,7 +402,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   } else if (!DENSE) {
     // ================= selector: one warp per query of the block
     const int q = warp - C::kSelWarp0;
-    uint64_t* pool = sPool + q * kPool;
+    uint64_t* pool = sPool + q * C::kPool;
     uint32_t* hist = sHist + q * 256;
     const int64_t t = t0 + q;
     const bool valid = t < p.T;
@@ -314,8 +412,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     uint64_t theta = 0ull;  // exact 512th best word so far (0 until 512 words were seen)
     int n = 0;              // words in the pool
     for (int it = 0; it < n_tiles; ++it) {
-      const int sb = it % kScoreBufs;
-      const uint32_t sph = (it / kScoreBufs) & 1;
+      const int sb = it % C::kScoreBufs;
+      const uint32_t sph = (it / C::kScoreBufs) & 1;
       if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
       const int64_t key0 = static_cast<int64_t>(tile_lo + it) * kTileKeys;
       const float* sc = sScore + (sb * NQ + q) * kTileKeys;
@@ -331,7 +429,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      if (n > kPool - kTileKeys) {
+      if (n > C::kPool - kTileKeys) {
         theta = select_compact<kTopK>(pool, n, hist, lane);
         n = kTopK;
       }
@@ -353,6 +451,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK + lane * R;
 #pragma unroll
         for (int r = 0; r < R; ++r) dst[r] = v[r];
+        __threadfence();  // the list is visible GPU-wide before this CTA takes its ticket
       } else {
         int32_t* oi = p.out_idx + row * kTopK + lane * R;
 #pragma unroll
@@ -373,32 +472,20 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-}
-
-// Combines per-split Top-512 lists (each sorted, packed) into the final output. One warp per
-// output row, pairwise bitonic merges in shared memory.
-__global__ void __launch_bounds__(128) merge_splits_kernel(const uint64_t* __restrict__ partial,
-                                                           int n_splits, int64_t n_rows,
-                                                           int32_t* __restrict__ out_idx,
-                                                           float* __restrict__ out_score) {
-  __shared__ uint64_t s_lists[4][2][kTopK];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t row = static_cast<int64_t>(blockIdx.x) * 4 + warp;
-  if (row >= n_rows) return;
-  uint64_t* acc = s_lists[warp][0];
-  uint64_t* nxt = s_lists[warp][1];
-  const uint64_t* src = partial + row * n_splits * kTopK;
-  for (int i = lane; i < kTopK; i += 32) acc[i] = src[i];
-  __syncwarp();
-  for (int sp = 1; sp < n_splits; ++sp) {
-    for (int i = lane; i < kTopK; i += 32) nxt[i] = src[sp * kTopK + i];
-    __syncwarp();
-    merge_lists<kTopK>(acc, nxt, lane);
-  }
-  for (int i = lane; i < kTopK; i += 32) {
-    const uint64_t u = acc[i];
-    out_idx[row * kTopK + i] = u ? key_index(u) : -1;
-    if (out_score) out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
+  if (!DENSE && p.n_splits > 1) {
+    // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
+    // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
+    uint32_t* ticket = p.counters + static_cast<int64_t>(b) * p.n_qb + qb;
+    if (threadIdx.x == 0) {
+      __threadfence();
+      *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (*s_last) {
+      __threadfence();
+      if (!*s_abort) merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), warp, lane);
+      if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
+    }
   }
 }
 

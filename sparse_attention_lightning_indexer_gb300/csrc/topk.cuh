@@ -44,17 +44,27 @@ __device__ __forceinline__ uint64_t umin64(uint64_t a, uint64_t b) { return a < 
 // only exact score ties ever reach the index bits.
 template <int K>
 __device__ __noinline__ uint64_t select_compact(uint64_t* pool, int n, uint32_t* hist, int lane) {
-  uint64_t prefix = 0ull;  // the digits fixed so far (bits above `shift`)
-  uint32_t need = K;       // rank of the K-th word among words matching `prefix`
-  int shift = 56;
-  for (;; shift -= 8) {
+  // Bits above the highest bit in which two pool words differ are common to all of them: the
+  // first digit starts right below that, so no pass is spent on a digit every word shares.
+  uint64_t diff = 0ull;
+  const uint64_t first = pool[0];
+  for (int i = lane; i < n; i += 32) diff |= pool[i] ^ first;
+  const uint32_t dlo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(diff));
+  const uint32_t dhi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(diff >> 32));
+  const int top = dhi ? 63 - __clz(dhi) : (dlo ? 31 - __clz(dlo) : 0);  // highest differing bit
+  int width = top + 1 < 8 ? top + 1 : 8;
+  int shift = top + 1 - width;                   // current digit: bits [shift, shift + width)
+  uint64_t prefix = shift + width >= 64 ? 0ull : (first & (~0ull << (shift + width)));
+  uint32_t need = K;  // rank of the K-th word among words matching `prefix`
+  for (;;) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) hist[lane * 8 + i] = 0u;
     __syncwarp();
-    const uint64_t hi_mask = shift == 56 ? 0ull : (~0ull << (shift + 8));
+    const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
+    const uint32_t dmask = (1u << width) - 1u;
     for (int i = lane; i < n; i += 32) {
       const uint64_t u = pool[i];
-      if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & 255u], 1u);
+      if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & dmask], 1u);
     }
     __syncwarp();
     // Lane l owns bins 8l..8l+7. above = number of matching words in higher bins.
@@ -91,6 +101,8 @@ __device__ __noinline__ uint64_t select_compact(uint64_t* pool, int n, uint32_t*
     prefix |= static_cast<uint64_t>(bin) << shift;
     need -= bin_above;
     if (bin_cnt == need || shift == 0) break;
+    width = shift < 8 ? shift : 8;
+    shift -= width;
     __syncwarp();
   }
   // Keep exactly the words whose digits down to `shift` are >= the cut.
@@ -147,6 +159,47 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[R], int lane) {
       }
     }
   }
+}
+
+// Sorts a bitonic sequence of 32*R register words (lane-major, as above) descending.
+template <int R>
+__device__ __forceinline__ void warp_bitonic_merge_desc(uint64_t (&v)[R], int lane) {
+  constexpr int N = 32 * R;
+#pragma unroll
+  for (int j = N >> 1; j > 0; j >>= 1) {
+    if (j >= R) {
+      const int lj = j / R;
+      const bool lower = (lane & lj) == 0;
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const uint64_t other = __shfl_xor_sync(0xffffffffu, v[r], lj);
+        v[r] = lower ? umax64(v[r], other) : umin64(v[r], other);
+      }
+    } else {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if ((r & j) == 0) {
+          const uint64_t a = v[r], b = v[r | j];
+          v[r] = umax64(a, b);
+          v[r | j] = umin64(a, b);
+        }
+      }
+    }
+  }
+}
+
+// a and b each hold 32*R words sorted descending (lane-major); afterwards a holds the 32*R
+// largest words of both, sorted descending. The elementwise max of a and reversed b is a
+// bitonic sequence that contains exactly those words.
+template <int R>
+__device__ __forceinline__ void warp_merge_desc(uint64_t (&a)[R], const uint64_t (&b)[R],
+                                                int lane) {
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    const uint64_t br = __shfl_xor_sync(0xffffffffu, b[R - 1 - r], 31);  // b[N-1-e]
+    a[r] = umax64(a[r], br);
+  }
+  warp_bitonic_merge_desc<R>(a, lane);
 }
 
 __device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {

@@ -32,7 +32,8 @@ ERR_SCRATCH_LIMIT = -7
 
 EXPORTS = ("ds4idx_create", "ds4idx_score_topk", "ds4idx_score_topk_batched",
            "ds4idx_score_dense_debug", "ds4idx_sync_status", "ds4idx_destroy",
-           "ds4idx_status_string", "ds4idx_version", "ds4idx_score_topk_batched_noalloc")
+           "ds4idx_status_string", "ds4idx_version", "ds4idx_score_topk_batched_noalloc",
+           "ds4idx_kernels_launched")
 
 _lock = threading.Lock()
 _lib = None
@@ -86,9 +87,16 @@ def load(path: str | None = None):
         lib.ds4idx_score_topk_batched_noalloc.argtypes = [i32, i32, vp, vp, vp, vp, i64, i64, vp,
                                                           i32, vp, vp, vp]
         lib.ds4idx_score_topk_batched_noalloc.restype = ctypes.c_int
+        lib.ds4idx_kernels_launched.argtypes = []
+        lib.ds4idx_kernels_launched.restype = ctypes.c_uint64
         if path is None:
             _lib = lib
         return lib
+
+
+def kernels_launched() -> int:
+    """Kernels the library has enqueued in this process (its own count, for benchmarks)."""
+    return int(load().ds4idx_kernels_launched())
 
 
 def status_string(status: int) -> str:

@@ -22,7 +22,7 @@ def lib():
 
 def declared():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^\s*(?:int|const char\s*\*)\s+(ds4idx_\w+)\s*\(", text, re.M)))
+    return sorted(set(re.findall(r"^\s*(?:int|uint64_t|const char\s*\*)\s+(ds4idx_\w+)\s*\(", text, re.M)))
 
 
 def test_header_declares_the_boundary():
@@ -44,6 +44,7 @@ def test_status_strings_and_version(lib):
         assert s and s != "unknown status", code
     assert lib.ds4idx_status_string(-99).decode() == "unknown status"
     assert lib.ds4idx_version() == (1 << 16)
+    assert lib.ds4idx_kernels_launched() == 0  # nothing launched without a device
 
 
 def _cfg(**kw):
