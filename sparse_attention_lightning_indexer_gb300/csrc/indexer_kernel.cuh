@@ -93,79 +93,88 @@ struct KCfg {
   static constexpr int kOffHist = kOffPool + (DENSE ? 0 : NQ * kPool * 8);
   static constexpr int kOffBar = kOffHist + (DENSE ? 0 : NQ * 256 * 4);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
-  static_assert(kWarps * kTopK * 8 <= kStages * kKBytes, "merge slots reuse the K stages");
+  static_assert(4 * kTopK * 8 <= kStages * kKBytes, "split merge reuses the K stages");
+  static_assert((kStages * kKBytes / 8 - 2 * kTopK) / kTopK >= 2, "split merge needs two lists per round");
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 16 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
 
 template <int R>
-__device__ __forceinline__ void load_list(uint64_t (&v)[R], const uint64_t* src, int lane) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src + lane * R);
+__device__ __forceinline__ void write_output(const KParams& p, int64_t row,
+                                             const uint64_t (&v)[R], int lane) {
+  int32_t* oi = p.out_idx + row * kTopK + lane * R;
 #pragma unroll
-  for (int i = 0; i < R / 2; ++i) {
-    const uint4 x = s4[i];
-    v[2 * i] = (static_cast<uint64_t>(x.y) << 32) | x.x;
-    v[2 * i + 1] = (static_cast<uint64_t>(x.w) << 32) | x.z;
+  for (int r = 0; r < R; ++r) oi[r] = v[r] ? key_index(v[r]) : -1;
+  if (p.out_score) {
+    float* os = p.out_score + row * kTopK + lane * R;
+#pragma unroll
+    for (int r = 0; r < R; ++r) os[r] = v[r] ? key_score(v[r]) : -__int_as_float(0x7f800000);
   }
 }
-template <int R>
-__device__ __forceinline__ void store_list(uint64_t* dst, const uint64_t (&v)[R], int lane) {
-  uint4* d4 = reinterpret_cast<uint4*>(dst + lane * R);
-#pragma unroll
-  for (int i = 0; i < R / 2; ++i)
-    d4[i] = make_uint4(static_cast<uint32_t>(v[2 * i]), static_cast<uint32_t>(v[2 * i] >> 32),
-                       static_cast<uint32_t>(v[2 * i + 1]),
-                       static_cast<uint32_t>(v[2 * i + 1] >> 32));
+
+// Split plans, part 1 (every CTA): reduce each query's pool to its 512 best with a CTA-wide
+// radix select and publish them, unordered, as this split's list.
+template <class C>
+__device__ void publish_split_lists(const KParams& p, int b, int64_t t0, int split,
+                                    uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
+                                    uint32_t* hist, uint32_t* scratch) {
+  for (int q = 0; q < C::kN / kHeads; ++q) {
+    const int64_t t = t0 + q;
+    if (t >= p.T) break;
+    const int cnt = cta_select<kTopK, C::kThreads>(pools + q * C::kPool, static_cast<int>(pool_n[q]),
+                                                   stage, hist, scratch);
+    const int64_t row = static_cast<int64_t>(b) * p.T + t;
+    uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
+    for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
+    __syncthreads();
+  }
+  __threadfence();  // the lists are visible GPU-wide before this CTA takes its ticket
 }
 
-// Merges the n_splits sorted Top-512 lists of each query of a block into the final output. All
-// warps of the CTA take part: warp w folds lists w, w+W, ... into registers, then the W partial
-// results are combined pairwise in shared memory (`slots`, W x 512 words).
+// Split plans, part 2 (the CTA that takes a block's last ticket): copy every split's list of
+// each query into shared memory with independent wide loads, radix-select the 512 best, sort
+// them once in registers and write the output row. Lists that do not fit at once are folded in
+// rounds (the 512 survivors of a round stay at the front of the gather area).
 template <class C>
-__device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* slots, int warp,
-                                  int lane) {
+__device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* stage,
+                                  uint32_t* hist, uint32_t* scratch, int warp, int lane) {
   constexpr int R = kTopK / 32;
-  constexpr int W = C::kWarps;
-  const int used = p.n_splits < W ? p.n_splits : W;  // slots that receive lists
+  constexpr int kStageWords = C::kStages * C::kKBytes / 8;
+  constexpr int kCap = kStageWords - kTopK;  // gather area; the last 512 words receive selects
+  constexpr int kListsPerRound = (kCap - kTopK) / kTopK;
+  uint64_t* sel = stage + kCap;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
     if (t >= p.T) break;
     const int64_t row = static_cast<int64_t>(b) * p.T + t;
     const uint64_t* lists = p.partial + row * p.n_splits * kTopK;
-    if (warp < used) {
-      uint64_t acc[R];
-      load_list<R>(acc, lists + warp * kTopK, lane);
-      for (int sp = warp + W; sp < p.n_splits; sp += W) {
-        uint64_t nxt[R];
-        load_list<R>(nxt, lists + sp * kTopK, lane);
-        warp_merge_desc<R>(acc, nxt, lane);
-      }
-      store_list<R>(slots + warp * kTopK, acc, lane);
-    }
-    __syncthreads();
-    for (int stride = 1; stride < used; stride *= 2) {
-      if (warp % (2 * stride) == 0 && warp + stride < used) {
-        uint64_t a[R], o[R];
-        load_list<R>(a, slots + warp * kTopK, lane);
-        load_list<R>(o, slots + (warp + stride) * kTopK, lane);
-        warp_merge_desc<R>(a, o, lane);
-        store_list<R>(slots + warp * kTopK, a, lane);
-      }
+    int n = 0;  // words already in the gather area (survivors of earlier rounds)
+    for (int sp0 = 0; sp0 < p.n_splits; sp0 += kListsPerRound) {
+      const int nl = p.n_splits - sp0 < kListsPerRound ? p.n_splits - sp0 : kListsPerRound;
+      const uint4* src = reinterpret_cast<const uint4*>(lists + static_cast<int64_t>(sp0) * kTopK);
+      uint4* dst = reinterpret_cast<uint4*>(stage + n);
+      const int n4 = nl * kTopK / 2;
+#pragma unroll 4
+      for (int i = threadIdx.x; i < n4; i += C::kThreads) dst[i] = src[i];
       __syncthreads();
+      n += nl * kTopK;
+      if (sp0 + nl < p.n_splits) {  // another round follows: keep only the 512 best
+        const int kept = cta_select<kTopK, C::kThreads>(stage, n, sel, hist, scratch);
+        // zero-padded to exactly 512 words, so the next round's copy stays 16-byte aligned
+        for (int i = threadIdx.x; i < kTopK; i += C::kThreads) stage[i] = i < kept ? sel[i] : 0ull;
+        __syncthreads();
+        n = kTopK;
+      }
     }
+    const int cnt = cta_select<kTopK, C::kThreads>(stage, n, sel, hist, scratch);
     if (warp == 0) {
       uint64_t v[R];
-      load_list<R>(v, slots, lane);
-      int32_t* oi = p.out_idx + row * kTopK + lane * R;
 #pragma unroll
-      for (int r = 0; r < R; ++r) oi[r] = v[r] ? key_index(v[r]) : -1;
-      if (p.out_score) {
-        float* os = p.out_score + row * kTopK + lane * R;
-#pragma unroll
-        for (int r = 0; r < R; ++r) os[r] = v[r] ? key_score(v[r]) : -__int_as_float(0x7f800000);
-      }
+      for (int r = 0; r < R; ++r) v[r] = lane * R + r < cnt ? sel[lane * R + r] : 0ull;
+      warp_sort_desc<R>(v, lane);
+      write_output<R>(p, row, v, lane);
     }
     __syncthreads();
   }
@@ -196,6 +205,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
   volatile uint32_t* s_last = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
+  uint32_t* s_scratch = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 16);  // 8 words
+  uint32_t* s_pool_n = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 48);   // [NQ] <= 4
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -417,15 +428,19 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
       const int64_t key0 = static_cast<int64_t>(tile_lo + it) * kTileKeys;
       const float* sc = sScore + (sb * NQ + q) * kTileKeys;
+      constexpr int kGroups = kTileKeys / 32;
+      uint64_t u[kGroups];
+      uint32_t m[kGroups];
 #pragma unroll
-      for (int r = 0; r < kTileKeys / 32; ++r) {
+      for (int r = 0; r < kGroups; ++r) {  // four independent 32-key groups
         const int64_t key = key0 + r * 32 + lane;
-        const uint64_t u = key < vis_end ? pack_key(sc[r * 32 + lane], static_cast<uint32_t>(key))
-                                         : 0ull;
-        const bool pass = u > theta;
-        const uint32_t m = __ballot_sync(0xffffffffu, pass);
-        if (pass) pool[n + __popc(m & lt_mask)] = u;
-        n += __popc(m);
+        u[r] = key < vis_end ? pack_key(sc[r * 32 + lane], static_cast<uint32_t>(key)) : 0ull;
+        m[r] = __ballot_sync(0xffffffffu, u[r] > theta);
+      }
+#pragma unroll
+      for (int r = 0; r < kGroups; ++r) {
+        if (u[r] > theta) pool[n + __popc(m[r] & lt_mask)] = u[r];
+        n += __popc(m[r]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
@@ -434,34 +449,22 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         n = kTopK;
       }
     }
-    if (n > kTopK) n = (select_compact<kTopK>(pool, n, hist, lane), kTopK);
-    __syncwarp();
-    // Final order: sort the (at most 512) survivors in registers, best first.
-    constexpr int R = kTopK / 32;
-    uint64_t v[R];
+    if (p.n_splits > 1) {
+      // Split plans finish with a CTA-wide select after the role loops (every warp helps).
+      if (lane == 0) s_pool_n[q] = static_cast<uint32_t>(n);
+    } else {
+      if (n > kTopK) n = (select_compact<kTopK>(pool, n, hist, lane), kTopK);
+      __syncwarp();
+      // Final order: sort the (at most 512) survivors in registers, best first.
+      constexpr int R = kTopK / 32;
+      uint64_t v[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-      const int i = lane * R + r;
-      v[r] = i < n ? pool[i] : 0ull;
-    }
-    warp_sort_desc<R>(v, lane);
-    if (valid && !*s_abort) {
-      const int64_t row = static_cast<int64_t>(b) * p.T + t;
-      if (p.n_splits > 1) {
-        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK + lane * R;
-#pragma unroll
-        for (int r = 0; r < R; ++r) dst[r] = v[r];
-        __threadfence();  // the list is visible GPU-wide before this CTA takes its ticket
-      } else {
-        int32_t* oi = p.out_idx + row * kTopK + lane * R;
-#pragma unroll
-        for (int r = 0; r < R; ++r) oi[r] = v[r] ? key_index(v[r]) : -1;
-        if (p.out_score) {
-          float* os = p.out_score + row * kTopK + lane * R;
-#pragma unroll
-          for (int r = 0; r < R; ++r) os[r] = v[r] ? key_score(v[r]) : -__int_as_float(0x7f800000);
-        }
+      for (int r = 0; r < R; ++r) {
+        const int i = lane * R + r;
+        v[r] = i < n ? pool[i] : 0ull;
       }
+      warp_sort_desc<R>(v, lane);
+      if (valid && !*s_abort) write_output<R>(p, static_cast<int64_t>(b) * p.T + t, v, lane);
     }
   }
 
@@ -476,6 +479,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
     uint32_t* ticket = p.counters + static_cast<int64_t>(b) * p.n_qb + qb;
+    if (!*s_abort)
+      publish_split_lists<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK),
+                             sHist, s_scratch);
     if (threadIdx.x == 0) {
       __threadfence();
       *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1u : 0u;
@@ -483,7 +489,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     __syncthreads();
     if (*s_last) {
       __threadfence();
-      if (!*s_abort) merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), warp, lane);
+      if (!*s_abort)
+        merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch, warp,
+                             lane);
       if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
     }
   }

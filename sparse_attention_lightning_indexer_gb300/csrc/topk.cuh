@@ -127,14 +127,33 @@ __device__ __noinline__ uint64_t select_compact(uint64_t* pool, int n, uint32_t*
   return mn;
 }
 
+// One in-register compare-exchange stage at distance J < R (element e = lane*R + r).
+template <int R, int J>
+__device__ __forceinline__ void reg_stage(uint64_t (&v)[R], int lane, int k) {
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    if ((r & J) == 0) {
+      const bool desc = ((lane * R + r) & k) == 0;
+      const uint64_t a = v[r], b = v[r | J];
+      const bool swap = desc ? (a < b) : (a > b);
+      v[r] = swap ? b : a;
+      v[r | J] = swap ? a : b;
+    }
+  }
+}
+
 // Bitonic sort, descending, of 32*R words held in registers by one warp, element e = lane*R + r.
-// Distances below R are register swaps; larger ones exchange through shuffles.
+// Distances below R are register swaps; larger ones exchange through shuffles. The stage loops
+// run at run time and only the per-register work is unrolled: a fully unrolled 512-word network
+// is thousands of straight-line instructions that would execute once, from a cold instruction
+// cache.
 template <int R>
 __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[R], int lane) {
+  static_assert(R == 16, "in-register stages are spelled out for 16 words per lane");
   constexpr int N = 32 * R;
-#pragma unroll
+#pragma unroll 1
   for (int k = 2; k <= N; k <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int j = k >> 1; j > 0; j >>= 1) {
       if (j >= R) {
         const int lj = j / R;
@@ -145,61 +164,132 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[R], int lane) {
           const bool desc = ((lane * R + r) & k) == 0;
           v[r] = (lower == desc) ? umax64(v[r], other) : umin64(v[r], other);
         }
+      } else if (j == 8) {
+        reg_stage<R, 8>(v, lane, k);
+      } else if (j == 4) {
+        reg_stage<R, 4>(v, lane, k);
+      } else if (j == 2) {
+        reg_stage<R, 2>(v, lane, k);
       } else {
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          if ((r & j) == 0) {
-            const bool desc = ((lane * R + r) & k) == 0;
-            const uint64_t a = v[r], b = v[r | j];
-            const bool swap = desc ? (a < b) : (a > b);
-            v[r] = swap ? b : a;
-            v[r | j] = swap ? a : b;
-          }
-        }
+        reg_stage<R, 1>(v, lane, k);
       }
     }
   }
 }
 
-// Sorts a bitonic sequence of 32*R register words (lane-major, as above) descending.
-template <int R>
-__device__ __forceinline__ void warp_bitonic_merge_desc(uint64_t (&v)[R], int lane) {
-  constexpr int N = 32 * R;
-#pragma unroll
-  for (int j = N >> 1; j > 0; j >>= 1) {
-    if (j >= R) {
-      const int lj = j / R;
-      const bool lower = (lane & lj) == 0;
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const uint64_t other = __shfl_xor_sync(0xffffffffu, v[r], lj);
-        v[r] = lower ? umax64(v[r], other) : umin64(v[r], other);
-      }
-    } else {
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if ((r & j) == 0) {
-          const uint64_t a = v[r], b = v[r | j];
-          v[r] = umax64(a, b);
-          v[r | j] = umin64(a, b);
-        }
-      }
+// CTA-wide variant of select_compact for the end of a kernel, when every warp is free. All NT
+// threads call it. pool[0..n) holds distinct non-zero words plus any number of zero words
+// (empty slots, ignored); `out` receives the min(K, #non-zero) largest words, unordered, and
+// that count is returned. hist: 256 shared words; scratch: 8 shared words.
+template <int K, int NT>
+__device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* out, uint32_t* hist,
+                          uint32_t* scratch) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  if (tid == 0) {
+    scratch[0] = 0u;
+    scratch[1] = 0u;
+    scratch[5] = 0u;
+    scratch[7] = 0u;
+  }
+  __syncthreads();
+  // One pass: non-zero count, and the bits in which non-zero words differ from a reference.
+  uint64_t ref = 0ull;
+  for (int i = 0; i < n && ref == 0ull; ++i) ref = pool[i];  // usually pool[0]
+  uint64_t diff = 0ull;
+  uint32_t nnz = 0u;
+  for (int i = tid; i < n; i += NT) {
+    const uint64_t u = pool[i];
+    if (u) {
+      diff |= u ^ ref;
+      ++nnz;
     }
   }
-}
-
-// a and b each hold 32*R words sorted descending (lane-major); afterwards a holds the 32*R
-// largest words of both, sorted descending. The elementwise max of a and reversed b is a
-// bitonic sequence that contains exactly those words.
-template <int R>
-__device__ __forceinline__ void warp_merge_desc(uint64_t (&a)[R], const uint64_t (&b)[R],
-                                                int lane) {
-#pragma unroll
-  for (int r = 0; r < R; ++r) {
-    const uint64_t br = __shfl_xor_sync(0xffffffffu, b[R - 1 - r], 31);  // b[N-1-e]
-    a[r] = umax64(a[r], br);
+  const uint32_t wlo = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(diff));
+  const uint32_t whi = __reduce_or_sync(0xffffffffu, static_cast<uint32_t>(diff >> 32));
+  const uint32_t wn = __reduce_add_sync(0xffffffffu, nnz);
+  if (lane == 0) {
+    atomicOr(&scratch[0], wlo);
+    atomicOr(&scratch[1], whi);
+    atomicAdd(&scratch[7], wn);
   }
-  warp_bitonic_merge_desc<R>(a, lane);
+  __syncthreads();
+  if (scratch[7] <= static_cast<uint32_t>(K)) {  // everything non-zero is kept
+    for (int base = 0; base < n; base += NT) {
+      const int i = base + tid;
+      const uint64_t u = i < n ? pool[i] : 0ull;
+      const uint32_t m = __ballot_sync(0xffffffffu, u != 0ull);
+      uint32_t slot = 0;
+      if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
+      slot = __shfl_sync(0xffffffffu, slot, 0);
+      if (u) out[slot + __popc(m & lt_mask)] = u;
+    }
+    __syncthreads();
+    return static_cast<int>(scratch[7]);
+  }
+  const uint64_t first = ref;
+  const uint32_t dlo = scratch[0], dhi = scratch[1];
+  const int top = dhi ? 63 - __clz(dhi) : (dlo ? 31 - __clz(dlo) : 0);
+  int width = top + 1 < 8 ? top + 1 : 8;
+  int shift = top + 1 - width;
+  uint64_t prefix = shift + width >= 64 ? 0ull : (first & (~0ull << (shift + width)));
+  uint32_t need = K;
+  for (;;) {
+    for (int i = tid; i < 256; i += NT) hist[i] = 0u;
+    __syncthreads();
+    const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
+    const uint32_t dmask = (1u << width) - 1u;
+    for (int i = tid; i < n; i += NT) {
+      const uint64_t u = pool[i];
+      if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & dmask], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = hist[lane * 8 + j];
+        sum += c[j];
+      }
+      uint32_t incl = sum;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const uint32_t v = __shfl_down_sync(0xffffffffu, incl, off);
+        if (lane + off < 32) incl += v;
+      }
+      uint32_t run = incl - sum;
+#pragma unroll
+      for (int j = 7; j >= 0; --j) {
+        if (run < need && run + c[j] >= need) {
+          scratch[2] = lane * 8 + j;
+          scratch[3] = run;
+          scratch[4] = c[j];
+        }
+        run += c[j];
+      }
+    }
+    __syncthreads();
+    const uint32_t bin = scratch[2], above = scratch[3], cnt = scratch[4];
+    __syncthreads();
+    prefix |= static_cast<uint64_t>(bin) << shift;
+    need -= above;
+    if (cnt == need || shift == 0) break;
+    width = shift < 8 ? shift : 8;
+    shift -= width;
+  }
+  const uint64_t cut = prefix >> shift;
+  for (int base = 0; base < n; base += NT) {
+    const int i = base + tid;
+    const uint64_t u = i < n ? pool[i] : 0ull;
+    const bool keep = i < n && (u >> shift) >= cut;
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    uint32_t slot = 0;
+    if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    if (keep) out[slot + __popc(m & lt_mask)] = u;
+  }
+  __syncthreads();
+  return K;
 }
 
 __device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {

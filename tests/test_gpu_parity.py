@@ -187,3 +187,22 @@ def test_unsupported_config():
     with pytest.raises(ds4idx.Ds4IdxError) as e:
         ds4idx.Indexer(ds4idx.BF16, max_T=16, max_S=16, n_heads=32)
     assert e.value.status == ds4idx.ERR_UNSUPPORTED
+
+
+def test_split_merge_concentrated_winners(fp8_ix, bf16_ix):
+    # 400 consecutive keys aligned with every query dominate the Top-512, so one or two key
+    # splits hold most of it: the prefix path of the split merge must see that its 64-word
+    # prefixes are not enough and fall back to the full merge.
+    for dtype, ix in ((inputs.FP8_E4M3, fp8_ix), (inputs.BF16, bf16_ix)):
+        prob = inputs.make("hot", T=1, S=30000, pos_offset=29999, seed=21, dtype=dtype)
+        prob.w.copy_(prob.w.abs())
+        if dtype == inputs.BF16:
+            prob.q.copy_(prob.q.abs())
+            prob.k[12000:12400] = (prob.k[12000:12400].float().abs() * 3.0).to(torch.bfloat16)
+        else:
+            prob.q.bitwise_and_(0x7F)  # clear E4M3 sign bits: |q|
+            prob.k[12000:12400] = prob.k[12000:12400].bitwise_and(0x7F)
+            prob.kscale[12000:12400] *= 3.0
+        stats, gi, _ = run_full(prob, ix)
+        hits = np.sum((gi[0] >= 12000) & (gi[0] < 12400))
+        assert hits > 300, hits  # the winners really are concentrated
