@@ -64,17 +64,24 @@ struct KCfg {
   static constexpr int kStepBytes = 32;                              // K bytes per MMA step
   // Depth of the epilogue -> selector score ring: it lets selectors fall behind by that many
   // tiles while they radix-select, without stalling the MMA pipeline.
-  static constexpr int kScoreBufs = NQ == 1 ? 16 : (DT == kDtFp8 ? 12 : 4);
+  static constexpr int kScoreBufs = NQ == 1 ? 16 : 12;
   // TMEM accumulators: all 512 columns, so a narrow (one-query) MMA can run up to 8 tiles
   // ahead of the epilogue instead of waiting on a round trip per tile.
   static constexpr int kAccBufs = 512 / kN;
-  // Per-query candidate pool (the kept 512 plus new candidates). One-query CTAs have the room
-  // for a pool that usually absorbs a whole key split without any intermediate select.
-  static constexpr int kPool = NQ == 1 ? 4096 : 1024;
-  static constexpr int kSelectors = DENSE ? 0 : NQ;
-  static constexpr int kEpiGroups = NQ >= 2 ? 2 : 1;        // warps per TMEM lane quadrant
-  static constexpr int kEpiWarps = 4 * kEpiGroups;
-  static constexpr int kQPerGroup = NQ / kEpiGroups;
+  // Candidate pool per selector warp (its kept 512 plus new candidates). One-query CTAs use two
+  // selector warps with 2048 words each, which usually absorb a whole decode split.
+  static constexpr int kPool = NQ == 1 ? 2048 : 1024;
+  // Epilogue: two warps per TMEM lane quadrant. With several queries the two groups split the
+  // queries; with one query they take alternate tiles.
+  static constexpr bool kEpiAltTiles = NQ == 1;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiPerTile = kEpiAltTiles ? 4 : 8;  // epilogue warps that handle a tile
+  static constexpr int kQPerGroup = kEpiAltTiles ? 1 : NQ / 2;
+  // Selectors: one warp per query, or two per query for a single query (each filters half of
+  // every tile's keys into its own pool).
+  static constexpr int kSelPerQuery = NQ == 1 ? 2 : 1;
+  static constexpr int kSelectors = DENSE ? 0 : NQ * kSelPerQuery;
+  static constexpr int kGroupsPerSel = (kTileKeys / 32) / kSelPerQuery;
   static constexpr int kTmaWarp = kEpiWarps;
   static constexpr int kMmaWarp = kEpiWarps + 1;
   static constexpr int kSelWarp0 = kEpiWarps + 2;
@@ -90,13 +97,13 @@ struct KCfg {
   static constexpr int kOffW = kOffK + kStages * kKBytes;
   static constexpr int kOffScore = kOffW + NQ * kHeads * 4;
   static constexpr int kOffPool = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
-  static constexpr int kOffHist = kOffPool + (DENSE ? 0 : NQ * kPool * 8);
-  static constexpr int kOffBar = kOffHist + (DENSE ? 0 : NQ * 256 * 4);
+  static constexpr int kOffHist = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
+  static constexpr int kOffBar = kOffHist + (DENSE ? 0 : kSelectors * 256 * 4);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
   static_assert(4 * kTopK * 8 <= kStages * kKBytes, "split merge reuses the K stages");
   static_assert((kStages * kKBytes / 8 - 2 * kTopK) / kTopK >= 2, "split merge needs two lists per round");
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 64 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffMisc + 96 + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
@@ -114,23 +121,40 @@ __device__ __forceinline__ void write_output(const KParams& p, int64_t row,
   }
 }
 
-// Split plans, part 1 (every CTA): reduce each query's pool to its 512 best with a CTA-wide
-// radix select and publish them, unordered, as this split's list.
+// CTA-wide finish (split plans, and one-query CTAs whose two selector warps keep separate
+// pools): for each query, the unused tails of its pools are zeroed (a CTA-wide select ignores
+// zero words), the 512 best words are radix-selected with all warps, and then either published
+// unordered as this split's list or sorted once and written as the output row.
 template <class C>
-__device__ void publish_split_lists(const KParams& p, int b, int64_t t0, int split,
-                                    uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
-                                    uint32_t* hist, uint32_t* scratch) {
+__device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split,
+                                  uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
+                                  uint32_t* hist, uint32_t* scratch, int warp, int lane) {
+  constexpr int R = kTopK / 32;
+  constexpr int kWords = C::kSelPerQuery * C::kPool;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
     if (t >= p.T) break;
-    const int cnt = cta_select<kTopK, C::kThreads>(pools + q * C::kPool, static_cast<int>(pool_n[q]),
-                                                   stage, hist, scratch);
+    uint64_t* base = pools + q * kWords;
+    for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
+      const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
+      for (int i = used + threadIdx.x; i < C::kPool; i += C::kThreads) base[sw * C::kPool + i] = 0ull;
+    }
+    __syncthreads();
+    const int cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
     const int64_t row = static_cast<int64_t>(b) * p.T + t;
-    uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
-    for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
+    if (p.n_splits > 1) {
+      uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
+      for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
+    } else if (warp == 0) {
+      uint64_t v[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) v[r] = lane * R + r < cnt ? stage[lane * R + r] : 0ull;
+      warp_sort_desc<R>(v, lane);
+      write_output<R>(p, row, v, lane);
+    }
     __syncthreads();
   }
-  __threadfence();  // the lists are visible GPU-wide before this CTA takes its ticket
+  if (p.n_splits > 1) __threadfence();  // lists visible GPU-wide before the ticket is taken
 }
 
 // Split plans, part 2 (the CTA that takes a block's last ticket): copy every split's list of
@@ -206,7 +230,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
   volatile uint32_t* s_last = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
   uint32_t* s_scratch = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 16);  // 8 words
-  uint32_t* s_pool_n = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 48);   // [NQ] <= 4
+  uint32_t* s_pool_n = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 48);   // [selectors]
+  // Running threshold published by each selector warp (only rises): a query's warps filter
+  // against the largest of them, which is still at most the CTA's exact 512th best.
+  volatile uint64_t* s_theta = reinterpret_cast<volatile uint64_t*>(smem + C::kOffMisc + 64);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -242,14 +269,15 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     }
     for (int i = 0; i < C::kAccBufs; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], C::kEpiWarps);
+      mbar_init(&tempty[i], C::kEpiPerTile);
     }
     for (int i = 0; i < C::kScoreBufs; ++i) {
-      mbar_init(&sfull[i], C::kEpiWarps);
-      mbar_init(&sempty[i], NQ);
+      mbar_init(&sfull[i], C::kEpiPerTile);
+      mbar_init(&sempty[i], C::kSelectors > 0 ? C::kSelectors : 1);  // unused without selectors
     }
     mbar_init(qfull, 1);
     *s_abort = 0u;
+    for (int i = 0; i < C::kSelectors; ++i) s_theta[i] = 0ull;
     fence_mbar_init();
   }
   if (warp == C::kTmaWarp && lane == 0) {
@@ -336,7 +364,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   } else if (warp < C::kEpiWarps) {
     // ================= epilogue: TMEM -> ReLU . w -> per-key score
     const int quad = warp & 3;
-    const int q0 = (warp >> 2) * C::kQPerGroup;
+    const int grp = warp >> 2;
+    const int q0 = C::kEpiAltTiles ? 0 : grp * C::kQPerGroup;
+    const int it0 = C::kEpiAltTiles ? grp : 0;   // first tile of this warp
+    const int step = C::kEpiAltTiles ? 2 : 1;    // tiles between this warp's tiles
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     // FP8 key scales are read two tiles ahead so their global-memory latency stays hidden
     // (decode streams the cache once, so these reads miss in L2).
@@ -347,10 +378,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     };
     float ks_next0 = 1.f, ks_next1 = 1.f;
     if (DT == kDtFp8) {
-      ks_next0 = load_scale(0);
-      ks_next1 = load_scale(1);
+      ks_next0 = load_scale(it0);
+      ks_next1 = load_scale(it0 + step);
     }
-    for (int it = 0; it < n_tiles; ++it) {
+    for (int it = it0; it < n_tiles; it += step) {
       const int acc = it % C::kAccBufs;
       const uint32_t aph = (it / C::kAccBufs) & 1;
       const int sb = it % C::kScoreBufs;
@@ -360,7 +391,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       if (DT == kDtFp8) {
         ks = ks_next0;
         ks_next0 = ks_next1;
-        ks_next1 = load_scale(it + 2);
+        ks_next1 = load_scale(it + 2 * step);
       }
       if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
       tc_fence_after();
@@ -411,47 +442,53 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
     }
   } else if (!DENSE) {
-    // ================= selector: one warp per query of the block
-    const int q = warp - C::kSelWarp0;
-    uint64_t* pool = sPool + q * C::kPool;
-    uint32_t* hist = sHist + q * 256;
+    // ================= selectors
+    const int sidx = warp - C::kSelWarp0;
+    const int q = sidx / C::kSelPerQuery;
+    const int g0 = (sidx % C::kSelPerQuery) * C::kGroupsPerSel;  // first 32-key group it filters
+    uint64_t* pool = sPool + sidx * C::kPool;
+    uint32_t* hist = sHist + sidx * 256;
     const int64_t t = t0 + q;
     const bool valid = t < p.T;
     const int64_t pt = pos_b + t;
     const int64_t vis_end = valid ? (pt < p.S - 1 ? pt : p.S - 1) + 1 : 0;
     const uint32_t lt_mask = (1u << lane) - 1u;
-    uint64_t theta = 0ull;  // exact 512th best word so far (0 until 512 words were seen)
+    uint64_t theta = 0ull;  // exact 512th best word this warp has seen (0 until 512 were seen)
     int n = 0;              // words in the pool
     for (int it = 0; it < n_tiles; ++it) {
       const int sb = it % C::kScoreBufs;
       const uint32_t sph = (it / C::kScoreBufs) & 1;
       if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
+      uint64_t th = theta;
+#pragma unroll
+      for (int o = 0; o < C::kSelPerQuery; ++o) th = umax64(th, s_theta[q * C::kSelPerQuery + o]);
       const int64_t key0 = static_cast<int64_t>(tile_lo + it) * kTileKeys;
       const float* sc = sScore + (sb * NQ + q) * kTileKeys;
-      constexpr int kGroups = kTileKeys / 32;
-      uint64_t u[kGroups];
-      uint32_t m[kGroups];
+      uint64_t u[C::kGroupsPerSel];
+      uint32_t m[C::kGroupsPerSel];
 #pragma unroll
-      for (int r = 0; r < kGroups; ++r) {  // four independent 32-key groups
-        const int64_t key = key0 + r * 32 + lane;
-        u[r] = key < vis_end ? pack_key(sc[r * 32 + lane], static_cast<uint32_t>(key)) : 0ull;
-        m[r] = __ballot_sync(0xffffffffu, u[r] > theta);
+      for (int r = 0; r < C::kGroupsPerSel; ++r) {  // independent 32-key groups
+        const int g = g0 + r;
+        const int64_t key = key0 + g * 32 + lane;
+        u[r] = key < vis_end ? pack_key(sc[g * 32 + lane], static_cast<uint32_t>(key)) : 0ull;
+        m[r] = __ballot_sync(0xffffffffu, u[r] > th);
       }
 #pragma unroll
-      for (int r = 0; r < kGroups; ++r) {
-        if (u[r] > theta) pool[n + __popc(m[r] & lt_mask)] = u[r];
+      for (int r = 0; r < C::kGroupsPerSel; ++r) {
+        if (u[r] > th) pool[n + __popc(m[r] & lt_mask)] = u[r];
         n += __popc(m[r]);
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sempty[sb]);
-      if (n > C::kPool - kTileKeys) {
+      if (n > C::kPool - C::kGroupsPerSel * 32) {
         theta = select_compact<kTopK>(pool, n, hist, lane);
         n = kTopK;
+        if (lane == 0) s_theta[sidx] = theta;
       }
     }
-    if (p.n_splits > 1) {
-      // Split plans finish with a CTA-wide select after the role loops (every warp helps).
-      if (lane == 0) s_pool_n[q] = static_cast<uint32_t>(n);
+    if (C::kSelPerQuery > 1 || p.n_splits > 1) {
+      // Finished with a CTA-wide select after the role loops (every warp helps).
+      if (lane == 0) s_pool_n[sidx] = static_cast<uint32_t>(n);
     } else {
       if (n > kTopK) n = (select_compact<kTopK>(pool, n, hist, lane), kTopK);
       __syncwarp();
@@ -475,13 +512,13 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
+  if (!DENSE && (C::kSelPerQuery > 1 || p.n_splits > 1) && !*s_abort)
+    finish_cta_select<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK), sHist,
+                         s_scratch, warp, lane);
   if (!DENSE && p.n_splits > 1) {
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
     uint32_t* ticket = p.counters + static_cast<int64_t>(b) * p.n_qb + qb;
-    if (!*s_abort)
-      publish_split_lists<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK),
-                             sHist, s_scratch);
     if (threadIdx.x == 0) {
       __threadfence();
       *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1u : 0u;
