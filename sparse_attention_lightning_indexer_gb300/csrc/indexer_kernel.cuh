@@ -68,18 +68,17 @@ struct KCfg {
   // TMEM accumulators: all 512 columns, so a narrow (one-query) MMA can run up to 8 tiles
   // ahead of the epilogue instead of waiting on a round trip per tile.
   static constexpr int kAccBufs = 512 / kN;
-  // Candidate pool per selector warp (its kept 512 plus new candidates). One-query CTAs use two
-  // selector warps with 2048 words each, which usually absorb a whole decode split.
-  static constexpr int kPool = NQ == 1 ? 2048 : 1024;
+  // Candidate pool per selector warp (its kept 512 plus new candidates).
+  static constexpr int kPool = 1024;
   // Epilogue: two warps per TMEM lane quadrant. With several queries the two groups split the
   // queries; with one query they take alternate tiles.
   static constexpr bool kEpiAltTiles = NQ == 1;
   static constexpr int kEpiWarps = 8;
   static constexpr int kEpiPerTile = kEpiAltTiles ? 4 : 8;  // epilogue warps that handle a tile
   static constexpr int kQPerGroup = kEpiAltTiles ? 1 : NQ / 2;
-  // Selectors: one warp per query, or two per query for a single query (each filters half of
-  // every tile's keys into its own pool).
-  static constexpr int kSelPerQuery = NQ == 1 ? 2 : 1;
+  // Selectors: one warp per query, or four for a single query (each filters one 32-key group of
+  // every tile into its own pool), which keeps a one-query CTA's selection at HBM pace.
+  static constexpr int kSelPerQuery = NQ == 1 ? 4 : 1;
   static constexpr int kSelectors = DENSE ? 0 : NQ * kSelPerQuery;
   static constexpr int kGroupsPerSel = (kTileKeys / 32) / kSelPerQuery;
   static constexpr int kTmaWarp = kEpiWarps;
@@ -398,41 +397,51 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       if (!DENSE) {
         if (!mbar_wait_warp(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
       }
-#pragma unroll 1
-      for (int q = q0; q < q0 + C::kQPerGroup; ++q) {
-        uint32_t r0[32], r1[32];
-        const uint32_t col = tmem + lane_base + static_cast<uint32_t>(acc * C::kN + q * kHeads);
-        tmem_ld32(col, r0);
-        tmem_ld32(col + 32, r1);
-        tmem_wait_ld();
-        // Four accumulator chains (heads = 0, 1, 2, 3 mod 4), two per packed fp32x2 FMA.
-        const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads);
-        uint64_t acc01 = 0ull, acc23 = 0ull;
+      // The warp's TMEM reads are 2 * kQPerGroup chunks of 32 head columns. Chunk c+1 is
+      // requested before chunk c is reduced, so each load's latency hides behind arithmetic
+      // (tcgen05.wait::ld waits for all outstanding loads; two 32-register buffers suffice).
+      constexpr int kChunks = 2 * C::kQPerGroup;
+      const uint32_t col0 = tmem + lane_base + static_cast<uint32_t>(acc * C::kN + q0 * kHeads);
+      uint32_t rb[2][32];
+      tmem_ld32(col0, rb[0]);
+      tmem_wait_ld();
+      uint64_t acc01 = 0ull, acc23 = 0ull;
 #pragma unroll
-        for (int h4 = 0; h4 < 16; ++h4) {
+      for (int c = 0; c < kChunks; ++c) {
+        if (c + 1 < kChunks) tmem_ld32(col0 + 32 * (c + 1), rb[(c + 1) & 1]);
+        const int q = q0 + c / 2;
+        // Four accumulator chains (heads = 0, 1, 2, 3 mod 4), two per packed fp32x2 FMA.
+        const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads + (c & 1) * 32);
+        const uint32_t* r = rb[c & 1];
+#pragma unroll
+        for (int h4 = 0; h4 < 8; ++h4) {
           const float4 wv = w4[h4];
-          const uint32_t* r = h4 < 8 ? r0 + 4 * h4 : r1 + 4 * (h4 - 8);
-          const float x0 = fmaxf(__uint_as_float(r[0]), 0.f);
-          const float x1 = fmaxf(__uint_as_float(r[1]), 0.f);
-          const float x2 = fmaxf(__uint_as_float(r[2]), 0.f);
-          const float x3 = fmaxf(__uint_as_float(r[3]), 0.f);
+          const float x0 = fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f);
+          const float x1 = fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f);
+          const float x2 = fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f);
+          const float x3 = fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f);
           acc01 = fma_f32x2(pack_f32x2(x0, x1), pack_f32x2(wv.x, wv.y), acc01);
           acc23 = fma_f32x2(pack_f32x2(x2, x3), pack_f32x2(wv.z, wv.w), acc23);
         }
-        float a0, a1, a2, a3;
-        unpack_f32x2(acc01, a0, a1);
-        unpack_f32x2(acc23, a2, a3);
-        float score = (a0 + a1) + (a2 + a3);
-        if (DT == kDtFp8) score *= ks;
-        if (DENSE) {
-          const int64_t t = t0 + q;
-          if (t < p.T && key < p.S) {
-            const bool vis = key <= pos_b + t;
-            p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
+        if (c & 1) {  // both halves of query q reduced
+          float a0, a1, a2, a3;
+          unpack_f32x2(acc01, a0, a1);
+          unpack_f32x2(acc23, a2, a3);
+          acc01 = 0ull;
+          acc23 = 0ull;
+          float score = (a0 + a1) + (a2 + a3);
+          if (DT == kDtFp8) score *= ks;
+          if (DENSE) {
+            const int64_t t = t0 + q;
+            if (t < p.T && key < p.S) {
+              const bool vis = key <= pos_b + t;
+              p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
+            }
+          } else {
+            sScore[(sb * NQ + q) * kTileKeys + quad * 32 + lane] = score;
           }
-        } else {
-          sScore[(sb * NQ + q) * kTileKeys + quad * 32 + lane] = score;
         }
+        if (c + 1 < kChunks) tmem_wait_ld();
       }
       tc_fence_before();
       __syncwarp();
