@@ -94,11 +94,18 @@ struct KCfg {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;
   static constexpr int kOffW = kOffK + kStages * kKBytes;
-  static constexpr int kOffScore = kOffW + NQ * kHeads * 4;
-  static constexpr int kOffPool = kOffScore + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
-  static constexpr int kOffHist = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
-  static constexpr int kOffBar = kOffHist + (DENSE ? 0 : kSelectors * 256 * 4);
+  static constexpr int kOffHist = kOffW + NQ * kHeads * 4;
+  static constexpr int kOffRing = kOffHist + (DENSE ? 0 : kSelectors * 256 * 4);
+  static constexpr int kOffPool = kOffRing + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
+  static constexpr int kOffSelEnd = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
+  // Buffered selection (one-query CTAs whose key split fits): the epilogue stores every fp32
+  // score of the split here and one CTA-wide select runs at the end. The buffer overlays the
+  // ring and the pools, which that mode leaves unused, plus whatever shared memory is left.
+  static constexpr int kBufTiles =
+      (NQ == 1 && !DENSE) ? (232448 - 1024 - 96 - kNumBars * 8 - kOffRing) / (kTileKeys * 4) : 0;
+  static constexpr int kOffBar = kOffSelEnd > kOffRing + kBufTiles * kTileKeys * 4
+                                     ? kOffSelEnd : kOffRing + kBufTiles * kTileKeys * 4;
   static_assert(4 * kTopK * 8 <= kStages * kKBytes, "split merge reuses the K stages");
   static_assert((kStages * kKBytes / 8 - 2 * kTopK) / kTopK >= 2, "split merge needs two lists per round");
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
@@ -124,22 +131,45 @@ __device__ __forceinline__ void write_output(const KParams& p, int64_t row,
 // pools): for each query, the unused tails of its pools are zeroed (a CTA-wide select ignores
 // zero words), the 512 best words are radix-selected with all warps, and then either published
 // unordered as this split's list or sorted once and written as the output row.
+// Buffered-mode words: the fp32 score of key key0 + i, packed, or 0 when the query cannot see it.
+struct ScoreWords {
+  const float* s;
+  int64_t key0, vis_end;
+  __device__ __forceinline__ uint64_t operator()(int i) const {
+    const int64_t key = key0 + i;
+    return key < vis_end ? pack_key(s[i], static_cast<uint32_t>(key)) : 0ull;
+  }
+};
+
 template <class C>
 __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split,
                                   uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
-                                  uint32_t* hist, uint32_t* scratch, int warp, int lane) {
+                                  uint32_t* hist, uint32_t* scratch, int warp, int lane,
+                                  const float* sbuf, int buffered_keys, int64_t key0,
+                                  int64_t pos_b) {
   constexpr int R = kTopK / 32;
   constexpr int kWords = C::kSelPerQuery * C::kPool;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
     if (t >= p.T) break;
-    uint64_t* base = pools + q * kWords;
-    for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
-      const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
-      for (int i = used + threadIdx.x; i < C::kPool; i += C::kThreads) base[sw * C::kPool + i] = 0ull;
+    int cnt;
+    if (buffered_keys > 0) {
+      const int64_t pt = pos_b + t;
+      const int64_t vis_end = (pt < p.S - 1 ? pt : p.S - 1) + 1;
+      constexpr int kStageWords = C::kStages * C::kKBytes / 8;
+      cnt = cta_select_sampled<kTopK, C::kThreads>(ScoreWords{sbuf, key0, vis_end}, buffered_keys,
+                                                   stage, stage + kTopK, kStageWords - kTopK,
+                                                   hist, scratch);
+    } else {
+      uint64_t* base = pools + q * kWords;
+      for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
+        const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
+        for (int i = used + threadIdx.x; i < C::kPool; i += C::kThreads)
+          base[sw * C::kPool + i] = 0ull;
+      }
+      __syncthreads();
+      cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
     }
-    __syncthreads();
-    const int cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
     const int64_t row = static_cast<int64_t>(b) * p.T + t;
     if (p.n_splits > 1) {
       uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
@@ -163,8 +193,7 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
 template <class C>
 __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* stage,
                                   uint32_t* hist, uint32_t* scratch, int warp, int lane) {
-  constexpr int R = kTopK / 32;
-  constexpr int kStageWords = C::kStages * C::kKBytes / 8;
+    constexpr int kStageWords = C::kStages * C::kKBytes / 8;
   constexpr int kCap = kStageWords - kTopK;  // gather area; the last 512 words receive selects
   constexpr int kListsPerRound = (kCap - kTopK) / kTopK;
   uint64_t* sel = stage + kCap;
@@ -179,7 +208,7 @@ __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t*
       const uint4* src = reinterpret_cast<const uint4*>(lists + static_cast<int64_t>(sp0) * kTopK);
       uint4* dst = reinterpret_cast<uint4*>(stage + n);
       const int n4 = nl * kTopK / 2;
-#pragma unroll 4
+#pragma unroll 8
       for (int i = threadIdx.x; i < n4; i += C::kThreads) dst[i] = src[i];
       __syncthreads();
       n += nl * kTopK;
@@ -191,13 +220,17 @@ __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t*
         n = kTopK;
       }
     }
-    const int cnt = cta_select<kTopK, C::kThreads>(stage, n, sel, hist, scratch);
-    if (warp == 0) {
-      uint64_t v[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) v[r] = lane * R + r < cnt ? sel[lane * R + r] : 0ull;
-      warp_sort_desc<R>(v, lane);
-      write_output<R>(p, row, v, lane);
+    // survivors of the sampled pre-filter go to the free words between the gather and `sel`
+    const int cnt = cta_select_sampled<kTopK, C::kThreads>(ArrayWords{stage}, n, sel, stage + n,
+                                                           kCap - n, hist, scratch);
+    // one CTA-wide sort of the 512 winners (zero-padded), then a coalesced store of the row
+    for (int i = cnt + threadIdx.x; i < kTopK; i += C::kThreads) sel[i] = 0ull;
+    __syncthreads();
+    cta_sort_desc<kTopK, C::kThreads>(sel);
+    for (int i = threadIdx.x; i < kTopK; i += C::kThreads) {
+      const uint64_t u = sel[i];
+      p.out_idx[row * kTopK + i] = u ? key_index(u) : -1;
+      if (p.out_score) p.out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
     }
     __syncthreads();
   }
@@ -214,7 +247,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sK = smem + C::kOffK;
   float* sW = reinterpret_cast<float*>(smem + C::kOffW);
-  float* sScore = reinterpret_cast<float*>(smem + C::kOffScore);
+  float* sScore = reinterpret_cast<float*>(smem + C::kOffRing);
+  float* sBuf = reinterpret_cast<float*>(smem + C::kOffRing);  // buffered mode only
   uint64_t* sPool = reinterpret_cast<uint64_t*>(smem + C::kOffPool);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -259,6 +293,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                                                               : tiles_total;
     n_tiles = hi > tile_lo ? hi - tile_lo : 0;
   }
+
+  const bool buffered = C::kBufTiles > 0 && n_tiles <= C::kBufTiles;
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
       if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
       tc_fence_after();
-      if (!DENSE) {
+      if (!DENSE && !buffered) {
         if (!mbar_wait_warp(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
       }
       // The warp's TMEM reads are 2 * kQPerGroup chunks of 32 head columns. Chunk c+1 is
@@ -437,6 +473,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
               const bool vis = key <= pos_b + t;
               p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
             }
+          } else if (buffered) {
+            sBuf[it * kTileKeys + quad * 32 + lane] = score;
           } else {
             sScore[(sb * NQ + q) * kTileKeys + quad * 32 + lane] = score;
           }
@@ -447,7 +485,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       __syncwarp();
       if (lane == 0) {
         mbar_arrive(&tempty[acc]);
-        if (!DENSE) mbar_arrive(&sfull[sb]);
+        if (!DENSE && !buffered) mbar_arrive(&sfull[sb]);
       }
     }
   } else if (!DENSE) {
@@ -464,7 +502,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     const uint32_t lt_mask = (1u << lane) - 1u;
     uint64_t theta = 0ull;  // exact 512th best word this warp has seen (0 until 512 were seen)
     int n = 0;              // words in the pool
-    for (int it = 0; it < n_tiles; ++it) {
+    for (int it = 0; it < (buffered ? 0 : n_tiles); ++it) {
       const int sb = it % C::kScoreBufs;
       const uint32_t sph = (it / C::kScoreBufs) & 1;
       if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
@@ -523,7 +561,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   }
   if (!DENSE && (C::kSelPerQuery > 1 || p.n_splits > 1) && !*s_abort)
     finish_cta_select<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK), sHist,
-                         s_scratch, warp, lane);
+                         s_scratch, warp, lane, sBuf, buffered ? n_tiles * kTileKeys : 0,
+                         static_cast<int64_t>(tile_lo) * kTileKeys, pos_b);
   if (!DENSE && p.n_splits > 1) {
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).

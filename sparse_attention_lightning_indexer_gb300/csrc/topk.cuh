@@ -178,12 +178,12 @@ __device__ __forceinline__ void warp_sort_desc(uint64_t (&v)[R], int lane) {
 }
 
 // CTA-wide variant of select_compact for the end of a kernel, when every warp is free. All NT
-// threads call it. pool[0..n) holds distinct non-zero words plus any number of zero words
-// (empty slots, ignored); `out` receives the min(K, #non-zero) largest words, unordered, and
-// that count is returned. hist: 256 shared words; scratch: 8 shared words.
-template <int K, int NT>
-__device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* out, uint32_t* hist,
-                          uint32_t* scratch) {
+// threads call it. get(i), i in [0, n), yields distinct non-zero words plus any number of zero
+// words (empty slots, ignored); `out` receives the min(K, #non-zero) largest words, unordered,
+// and that count is returned. hist: 256 shared words; scratch: 8 shared words.
+template <int K, int NT, class Get>
+__device__ __noinline__ int cta_select_get(const Get get, int n, uint64_t* out, uint32_t* hist,
+                                           uint32_t* scratch) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const uint32_t lt_mask = (1u << lane) - 1u;
   if (tid == 0) {
@@ -195,11 +195,11 @@ __device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* ou
   __syncthreads();
   // One pass: non-zero count, and the bits in which non-zero words differ from a reference.
   uint64_t ref = 0ull;
-  for (int i = 0; i < n && ref == 0ull; ++i) ref = pool[i];  // usually pool[0]
+  for (int i = 0; i < n && ref == 0ull; ++i) ref = get(i);  // usually word 0
   uint64_t diff = 0ull;
   uint32_t nnz = 0u;
   for (int i = tid; i < n; i += NT) {
-    const uint64_t u = pool[i];
+    const uint64_t u = get(i);
     if (u) {
       diff |= u ^ ref;
       ++nnz;
@@ -217,7 +217,7 @@ __device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* ou
   if (scratch[7] <= static_cast<uint32_t>(K)) {  // everything non-zero is kept
     for (int base = 0; base < n; base += NT) {
       const int i = base + tid;
-      const uint64_t u = i < n ? pool[i] : 0ull;
+      const uint64_t u = i < n ? get(i) : 0ull;
       const uint32_t m = __ballot_sync(0xffffffffu, u != 0ull);
       uint32_t slot = 0;
       if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
@@ -240,7 +240,7 @@ __device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* ou
     const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
     const uint32_t dmask = (1u << width) - 1u;
     for (int i = tid; i < n; i += NT) {
-      const uint64_t u = pool[i];
+      const uint64_t u = get(i);
       if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & dmask], 1u);
     }
     __syncthreads();
@@ -280,7 +280,7 @@ __device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* ou
   const uint64_t cut = prefix >> shift;
   for (int base = 0; base < n; base += NT) {
     const int i = base + tid;
-    const uint64_t u = i < n ? pool[i] : 0ull;
+    const uint64_t u = i < n ? get(i) : 0ull;
     const bool keep = i < n && (u >> shift) >= cut;
     const uint32_t m = __ballot_sync(0xffffffffu, keep);
     uint32_t slot = 0;
@@ -290,6 +290,94 @@ __device__ __noinline__ int cta_select(const uint64_t* pool, int n, uint64_t* ou
   }
   __syncthreads();
   return K;
+}
+
+struct ArrayWords {
+  const uint64_t* p;
+  __device__ __forceinline__ uint64_t operator()(int i) const { return p[i]; }
+};
+
+// cta_select_get with a sampled pre-filter, for large inputs. 128 evenly spaced words are
+// sampled and the kRank-th largest of them becomes a provisional cut; one pass keeps every word
+// >= that cut in `tmp` (capacity `cap` words). When at least K words survive, the K largest of
+// all words are among them and the radix select runs on the survivors only (about 3K words
+// instead of n); otherwise it runs on all n words. Exact either way.
+template <int K, int NT, class Get>
+__device__ __noinline__ int cta_select_sampled(const Get get, int n, uint64_t* out, uint64_t* tmp,
+                                               int cap, uint32_t* hist, uint32_t* scratch) {
+  constexpr int kSamples = 128;
+  static_assert(NT >= kSamples, "one sample per thread");
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int rank = static_cast<int>((3ll * K * kSamples) / (n > 1 ? n : 1));  // 0-based
+  if (n <= 4 * K || rank >= kSamples - 1 || cap < 4 * K + kSamples)
+    return cta_select_get<K, NT>(get, n, out, hist, scratch);
+  uint64_t* samples = tmp + cap - kSamples;  // top of tmp; survivors fill it from the bottom
+  if (tid == 0) {
+    scratch[6] = 0u;  // provisional cut, low and high halves
+    scratch[7] = 0u;
+    scratch[5] = 0u;  // survivor count
+  }
+  if (tid < kSamples) samples[tid] = get(static_cast<int>((static_cast<int64_t>(tid) * n) / kSamples));
+  __syncthreads();
+  if (tid < kSamples) {
+    const uint64_t mine = samples[tid];
+    int greater = 0;
+    for (int j = 0; j < kSamples; ++j) greater += samples[j] > mine ? 1 : 0;
+    if (greater == rank && mine != 0ull) {  // distinct non-zero words: at most one thread
+      scratch[6] = static_cast<uint32_t>(mine);
+      scratch[7] = static_cast<uint32_t>(mine >> 32);
+    }
+  }
+  __syncthreads();
+  const uint64_t cut = (static_cast<uint64_t>(scratch[7]) << 32) | scratch[6];
+  if (cut == 0ull) return cta_select_get<K, NT>(get, n, out, hist, scratch);
+  const int limit = cap - kSamples;
+  for (int base = 0; base < n; base += NT) {
+    const int i = base + tid;
+    const uint64_t u = i < n ? get(i) : 0ull;
+    const bool keep = u >= cut && u != 0ull;
+    const uint32_t m = __ballot_sync(0xffffffffu, keep);
+    uint32_t slot = 0;
+    if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
+    slot = __shfl_sync(0xffffffffu, slot, 0);
+    const uint32_t at = slot + __popc(m & ((1u << lane) - 1u));
+    if (keep && at < static_cast<uint32_t>(limit)) tmp[at] = u;
+  }
+  __syncthreads();
+  const int kept = static_cast<int>(scratch[5]);
+  __syncthreads();
+  if (kept < K || kept > limit) return cta_select_get<K, NT>(get, n, out, hist, scratch);
+  return cta_select_get<K, NT>(ArrayWords{tmp}, kept, out, hist, scratch);
+}
+
+// Bitonic sort, descending, of x[0..N) in shared memory by all NT threads of the CTA (for the
+// end of a kernel, when every warp is free): N/2 compare-exchanges per stage, one barrier each.
+template <int N, int NT>
+__device__ __forceinline__ void cta_sort_desc(uint64_t* x) {
+#pragma unroll 1
+  for (int k = 2; k <= N; k <<= 1) {
+#pragma unroll 1
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int p = threadIdx.x; p < N / 2; p += NT) {
+        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
+        const int l = i + j;
+        const uint64_t a = x[i], b = x[l];
+        const bool desc = (i & k) == 0;
+        if (desc ? (a < b) : (a > b)) {
+          x[i] = b;
+          x[l] = a;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// cta_select_get over an array of words.
+template <int K, int NT>
+__device__ __forceinline__ int cta_select(const uint64_t* pool, int n, uint64_t* out,
+                                          uint32_t* hist, uint32_t* scratch) {
+  return cta_select_get<K, NT>(ArrayWords{pool}, n, out, hist, scratch);
 }
 
 __device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {
