@@ -193,7 +193,7 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
 template <class C>
 __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* stage,
                                   uint32_t* hist, uint32_t* scratch, int warp, int lane) {
-    constexpr int kStageWords = C::kStages * C::kKBytes / 8;
+  constexpr int kStageWords = C::kStages * C::kKBytes / 8;
   constexpr int kCap = kStageWords - kTopK;  // gather area; the last 512 words receive selects
   constexpr int kListsPerRound = (kCap - kTopK) / kTopK;
   uint64_t* sel = stage + kCap;

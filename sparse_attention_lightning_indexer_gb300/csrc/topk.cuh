@@ -198,6 +198,7 @@ __device__ __noinline__ int cta_select_get(const Get get, int n, uint64_t* out, 
   for (int i = 0; i < n && ref == 0ull; ++i) ref = get(i);  // usually word 0
   uint64_t diff = 0ull;
   uint32_t nnz = 0u;
+#pragma unroll 4
   for (int i = tid; i < n; i += NT) {
     const uint64_t u = get(i);
     if (u) {
@@ -239,6 +240,7 @@ __device__ __noinline__ int cta_select_get(const Get get, int n, uint64_t* out, 
     __syncthreads();
     const uint64_t hi_mask = shift + width >= 64 ? 0ull : (~0ull << (shift + width));
     const uint32_t dmask = (1u << width) - 1u;
+#pragma unroll 4
     for (int i = tid; i < n; i += NT) {
       const uint64_t u = get(i);
       if ((u & hi_mask) == prefix) atomicAdd(&hist[static_cast<uint32_t>(u >> shift) & dmask], 1u);
@@ -277,16 +279,43 @@ __device__ __noinline__ int cta_select_get(const Get get, int n, uint64_t* out, 
     width = shift < 8 ? shift : 8;
     shift -= width;
   }
+  // Compaction in two passes (count per warp, then write at the warp's prefix offset), so no
+  // pass waits on a returning atomic. Each warp owns a contiguous stripe of the input.
   const uint64_t cut = prefix >> shift;
-  for (int base = 0; base < n; base += NT) {
-    const int i = base + tid;
-    const uint64_t u = i < n ? get(i) : 0ull;
-    const bool keep = i < n && (u >> shift) >= cut;
-    const uint32_t m = __ballot_sync(0xffffffffu, keep);
-    uint32_t slot = 0;
-    if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
-    slot = __shfl_sync(0xffffffffu, slot, 0);
-    if (keep) out[slot + __popc(m & lt_mask)] = u;
+  constexpr int kWarps = NT / 32;
+  const int per_warp = (n + kWarps - 1) / kWarps;
+  const int lo = warp * per_warp, hi = lo + per_warp < n ? lo + per_warp : n;
+  uint32_t cnt = 0;
+  for (int base = lo; base < hi; base += 128) {  // four independent words per lane
+    bool keep[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = base + r * 32 + lane;
+      keep[r] = i < hi && (get(i) >> shift) >= cut;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) cnt += __popc(__ballot_sync(0xffffffffu, keep[r]));
+  }
+  uint32_t* wcount = hist;  // the histogram is no longer needed
+  if (lane == 0) wcount[warp] = cnt;
+  __syncthreads();
+  uint32_t pos = 0;
+  for (int w = 0; w < warp; ++w) pos += wcount[w];
+  for (int base = lo; base < hi; base += 128) {
+    uint64_t u[4];
+    bool keep[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = base + r * 32 + lane;
+      u[r] = i < hi ? get(i) : 0ull;
+      keep[r] = i < hi && (u[r] >> shift) >= cut;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const uint32_t m = __ballot_sync(0xffffffffu, keep[r]);
+      if (keep[r]) out[pos + __popc(m & lt_mask)] = u[r];
+      pos += __popc(m);
+    }
   }
   __syncthreads();
   return K;
@@ -298,14 +327,16 @@ struct ArrayWords {
 };
 
 // cta_select_get with a sampled pre-filter, for large inputs. 128 evenly spaced words are
-// sampled and the kRank-th largest of them becomes a provisional cut; one pass keeps every word
-// >= that cut in `tmp` (capacity `cap` words). When at least K words survive, the K largest of
-// all words are among them and the radix select runs on the survivors only (about 3K words
-// instead of n); otherwise it runs on all n words. Exact either way.
+// sampled and a high-ranked one (about 3K/n of the way down) becomes a provisional cut; one pass
+// keeps every word >= that cut in per-warp segments of `tmp` (capacity `cap` words). When at
+// least K words survive and no segment overflows, the K largest of all words are among them
+// and the radix select runs on the segments only (about 3K words instead of n); otherwise it
+// runs on all n words. Exact either way.
 template <int K, int NT, class Get>
 __device__ __noinline__ int cta_select_sampled(const Get get, int n, uint64_t* out, uint64_t* tmp,
                                                int cap, uint32_t* hist, uint32_t* scratch) {
   constexpr int kSamples = 128;
+  constexpr int kMaxSeg = 256;  // survivor slots per warp (expected ~3K / warps)
   static_assert(NT >= kSamples, "one sample per thread");
   const int tid = threadIdx.x, lane = tid & 31;
   const int rank = static_cast<int>((3ll * K * kSamples) / (n > 1 ? n : 1));  // 0-based
@@ -316,12 +347,14 @@ __device__ __noinline__ int cta_select_sampled(const Get get, int n, uint64_t* o
     scratch[6] = 0u;  // provisional cut, low and high halves
     scratch[7] = 0u;
     scratch[5] = 0u;  // survivor count
+    scratch[4] = 0u;  // segment overflow flag
   }
   if (tid < kSamples) samples[tid] = get(static_cast<int>((static_cast<int64_t>(tid) * n) / kSamples));
   __syncthreads();
   if (tid < kSamples) {
     const uint64_t mine = samples[tid];
     int greater = 0;
+#pragma unroll 8
     for (int j = 0; j < kSamples; ++j) greater += samples[j] > mine ? 1 : 0;
     if (greater == rank && mine != 0ull) {  // distinct non-zero words: at most one thread
       scratch[6] = static_cast<uint32_t>(mine);
@@ -331,23 +364,43 @@ __device__ __noinline__ int cta_select_sampled(const Get get, int n, uint64_t* o
   __syncthreads();
   const uint64_t cut = (static_cast<uint64_t>(scratch[7]) << 32) | scratch[6];
   if (cut == 0ull) return cta_select_get<K, NT>(get, n, out, hist, scratch);
-  const int limit = cap - kSamples;
-  for (int base = 0; base < n; base += NT) {
-    const int i = base + tid;
-    const uint64_t u = i < n ? get(i) : 0ull;
-    const bool keep = u >= cut && u != 0ull;
-    const uint32_t m = __ballot_sync(0xffffffffu, keep);
-    uint32_t slot = 0;
-    if (lane == 0 && m) slot = atomicAdd(&scratch[5], __popc(m));
-    slot = __shfl_sync(0xffffffffu, slot, 0);
-    const uint32_t at = slot + __popc(m & ((1u << lane) - 1u));
-    if (keep && at < static_cast<uint32_t>(limit)) tmp[at] = u;
+  // Survivors go to per-warp segments of kSeg zero-initialised words (a register counter per
+  // warp, no atomics); the select then reads every segment and ignores the zero slots.
+  constexpr int kWarps = NT / 32;
+  const int seg = (cap - kSamples) / kWarps < kMaxSeg ? (cap - kSamples) / kWarps : kMaxSeg;
+  const int warp = tid >> 5;
+  for (int i = tid; i < kWarps * seg; i += NT) tmp[i] = 0ull;
+  __syncthreads();
+  uint64_t* mine = tmp + warp * seg;
+  const int per_warp = (n + kWarps - 1) / kWarps;
+  const int lo = warp * per_warp, hi = lo + per_warp < n ? lo + per_warp : n;
+  uint32_t cnt = 0;
+  for (int base = lo; base < hi; base += 128) {  // four independent words per lane
+    uint64_t u[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = base + r * 32 + lane;
+      u[r] = i < hi ? get(i) : 0ull;
+    }
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const bool keep = u[r] >= cut && u[r] != 0ull;
+      const uint32_t m = __ballot_sync(0xffffffffu, keep);
+      const uint32_t at = cnt + __popc(m & ((1u << lane) - 1u));
+      if (keep && at < static_cast<uint32_t>(seg)) mine[at] = u[r];
+      cnt += __popc(m);
+    }
+  }
+  if (lane == 0) {
+    atomicAdd(&scratch[5], cnt);
+    if (cnt > static_cast<uint32_t>(seg)) atomicOr(&scratch[4], 1u);  // a segment overflowed
   }
   __syncthreads();
   const int kept = static_cast<int>(scratch[5]);
+  const bool overflow = scratch[4] != 0u;
   __syncthreads();
-  if (kept < K || kept > limit) return cta_select_get<K, NT>(get, n, out, hist, scratch);
-  return cta_select_get<K, NT>(ArrayWords{tmp}, kept, out, hist, scratch);
+  if (kept < K || overflow) return cta_select_get<K, NT>(get, n, out, hist, scratch);
+  return cta_select_get<K, NT>(ArrayWords{tmp}, kWarps * seg, out, hist, scratch);
 }
 
 // Bitonic sort, descending, of x[0..N) in shared memory by all NT threads of the CTA (for the
