@@ -100,7 +100,9 @@ Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
 }
 
 size_t plan_partial_words(const Plan& pl, int64_t B, int64_t T) {
-  return pl.n_splits > 1 ? static_cast<size_t>(B * T) * pl.n_splits * kTopK : 0;
+  // one-query CTAs publish a slot per split (count window + candidates), others 512 words
+  const size_t per_split = pl.nq == 1 ? static_cast<size_t>(kSlotWords) : static_cast<size_t>(kTopK);
+  return pl.n_splits > 1 ? static_cast<size_t>(B * T) * pl.n_splits * per_split : 0;
 }
 size_t plan_counters(const Plan& pl, int64_t B) {
   return pl.n_splits > 1 ? static_cast<size_t>(B) * pl.n_qb : 0;

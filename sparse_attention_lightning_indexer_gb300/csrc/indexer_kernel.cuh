@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <cuda.h>
 
+#include "histsel.cuh"
 #include "ptx.cuh"
 #include "topk.cuh"
 
@@ -38,12 +39,51 @@ constexpr int kMaxBatch = 64;
 constexpr int kDtBf16 = 0;
 constexpr int kDtFp8 = 1;
 
+// ---- one-query split plans: slot format of a split's published list
+// A split publishes, in a slot of kSlotWords words:
+//   word 0        count m | window start lo << 32 | window width nb << 48
+//   words 2..129  a window of 256 32-bit counts of the published words per bin (histsel.cuh),
+//                 bins lo .. lo + nb - 1; bins below the window may go uncounted (an undercount
+//                 can only lower the merge's cut bin, never drop a winner)
+//   words 130..   the m published words, unordered (m <= kSlotListCap)
+// A split publishes every word of its keys whose bin is at or above a bin that at least 512 of
+// its words reach: a superset of its 512 best, hence of every global winner among its keys.
+constexpr int kSlotHdrWords = 2;
+constexpr int kSlotHistBins = 256;
+constexpr int kSlotListOff = kSlotHdrWords + kSlotHistBins / 2;
+constexpr int kSlotWords = 1152;
+constexpr int kSlotListCap = kSlotWords - kSlotListOff;
+constexpr int kSurvCap = 2048;   // words the bin-ranked final selection takes at most
+constexpr int kRankBins = 1024;  // bins it spans at most
+constexpr int kRecut = 256;      // new candidates between two raises of the epilogue's cut bin
+
+// Shared-memory scratch of the bin-ranked final selection and of the slot merge.
+struct RankArea {
+  static constexpr int kBytes = 2 * kSurvCap * 8 + 3 * kRankBins * 4 + 256 * 4 + 512 * 4;
+  uint64_t* sv;      // [kSurvCap] words to rank
+  uint64_t* sorted;  // [kSurvCap] the same words grouped by bin, best bin first
+  uint32_t* cnt;     // [kRankBins] words per bin
+  uint32_t* off;     // [kRankBins] first position of each bin
+  uint32_t* cur;     // [kRankBins] scatter cursors
+  uint32_t* rhist;   // [256] radix-select scratch
+  uint32_t* hdr;     // [512] merge headers
+  __device__ explicit RankArea(uint8_t* base)
+      : sv(reinterpret_cast<uint64_t*>(base)),
+        sorted(reinterpret_cast<uint64_t*>(base) + kSurvCap),
+        cnt(reinterpret_cast<uint32_t*>(base + 2 * kSurvCap * 8)),
+        off(cnt + kRankBins),
+        cur(off + kRankBins),
+        rhist(cur + kRankBins),
+        hdr(rhist + 256) {}
+};
+
 struct KParams {
   const float* w;        // [B, T, 64]
   const float* kscale;   // [B, S] (FP8) or null
   int32_t* out_idx;      // [B, T, 512]
   float* out_score;      // [B, T, 512] or null
-  uint64_t* partial;     // [B, T, n_splits, 512] packed lists when n_splits > 1
+  uint64_t* partial;     // per-split lists when n_splits > 1: [B, T, n_splits, 512] words, or
+                         // [B, n_splits, kSlotWords] slots for one-query CTAs
   uint32_t* counters;    // [B * n_qb] split tickets (zero between calls) when n_splits > 1
   float* dense;          // [T, S] scores (debug variant)
   uint32_t* err;         // device error word
@@ -99,17 +139,29 @@ struct KCfg {
   static constexpr int kOffPool = kOffRing + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
   static constexpr int kOffSelEnd = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
-  // Buffered selection (one-query CTAs whose key split fits): the epilogue stores every fp32
-  // score of the split here and one CTA-wide select runs at the end. The buffer overlays the
-  // ring and the pools, which that mode leaves unused, plus whatever shared memory is left.
+  static constexpr int kMiscBytes = 128;
+  // Buffered selection (one-query CTAs whose key split fits): the epilogue keeps every fp32
+  // score of the split, a bitmap of the keys that beat its running cut bin, and 16-bit per-bin
+  // counts of those keys; the final selection reads them back (finish_hist). These overlay the
+  // selector histograms, the ring and the pools, which that mode leaves unused, plus whatever
+  // shared memory is left.
+  static constexpr bool kHistSel = NQ == 1 && !DENSE;
+  static constexpr int kBinsBytes = kHBins * 2;
   static constexpr int kBufTiles =
-      (NQ == 1 && !DENSE) ? (232448 - 1024 - 96 - kNumBars * 8 - kOffRing) / (kTileKeys * 4) : 0;
-  static constexpr int kOffBar = kOffSelEnd > kOffRing + kBufTiles * kTileKeys * 4
-                                     ? kOffSelEnd : kOffRing + kBufTiles * kTileKeys * 4;
+      kHistSel ? (232448 - 1024 - kMiscBytes - kNumBars * 8 - kOffHist - kBinsBytes) /
+                     (kTileKeys * 4 + 16)
+               : 0;
+  static constexpr int kOffBins = kOffHist;
+  static constexpr int kOffBits = kOffBins + kBinsBytes;
+  static constexpr int kOffBuf = kOffBits + kBufTiles * 16;
+  static constexpr int kBufEnd = kHistSel ? kOffBuf + kBufTiles * kTileKeys * 4 : 0;
+  static constexpr int kOffBar = kOffSelEnd > kBufEnd ? kOffSelEnd : kBufEnd;
+  static_assert(!kHistSel || kOffBar - kOffHist >= RankArea::kBytes, "slot merge area");
+  static_assert(!kHistSel || kStages * kKBytes >= RankArea::kBytes, "final ranking area");
   static_assert(4 * kTopK * 8 <= kStages * kKBytes, "split merge reuses the K stages");
   static_assert((kStages * kKBytes / 8 - 2 * kTopK) / kTopK >= 2, "split merge needs two lists per round");
   static constexpr int kOffMisc = kOffBar + kNumBars * 8;
-  static constexpr int kSmemBytes = kOffMisc + 96 + 1024;  // + alignment slack
+  static constexpr int kSmemBytes = kOffMisc + kMiscBytes + 1024;  // + alignment slack
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kQBytes % 1024 == 0 && kKBytes % 1024 == 0, "swizzle atoms need 1 KiB alignment");
 };
@@ -127,53 +179,65 @@ __device__ __forceinline__ void write_output(const KParams& p, int64_t row,
   }
 }
 
-// CTA-wide finish (split plans, and one-query CTAs whose two selector warps keep separate
-// pools): for each query, the unused tails of its pools are zeroed (a CTA-wide select ignores
-// zero words), the 512 best words are radix-selected with all warps, and then either published
-// unordered as this split's list or sorted once and written as the output row.
-// Buffered-mode words: the fp32 score of key key0 + i, packed, or 0 when the query cannot see it.
-struct ScoreWords {
-  const float* s;
-  int64_t key0, vis_end;
-  __device__ __forceinline__ uint64_t operator()(int i) const {
-    const int64_t key = key0 + i;
-    return key < vis_end ? pack_key(s[i], static_cast<uint32_t>(key)) : 0ull;
+// Publishes cnt (<= 512) words as a one-query split's slot, with a histogram window counted
+// from the words themselves (the 256 bins up to the highest bin present). `tmp`: 256 words.
+template <int NT>
+__device__ void publish_slot(uint64_t* slot, const uint64_t* words, int cnt, uint32_t* tmp,
+                             uint32_t* scratch, int lane) {
+  if (threadIdx.x == 0) scratch[0] = 0u;
+  for (int i = threadIdx.x; i < kSlotHistBins; i += NT) tmp[i] = 0u;
+  __syncthreads();
+  uint32_t mb = 0u;
+  for (int i = threadIdx.x; i < cnt; i += NT) mb = max(mb, hbin(words[i]));
+  mb = __reduce_max_sync(0xffffffffu, mb);
+  if (lane == 0 && mb) atomicMax(&scratch[0], mb);
+  __syncthreads();
+  const uint32_t hi = scratch[0];
+  const uint32_t lo = hi >= kSlotHistBins - 1 ? hi - (kSlotHistBins - 1) : 0u;
+  for (int i = threadIdx.x; i < cnt; i += NT) {
+    const uint32_t bn = hbin(words[i]);
+    if (bn >= lo) atomicAdd(&tmp[bn - lo], 1u);
   }
-};
+  __syncthreads();
+  const uint32_t nb = cnt > 0 ? hi - lo + 1 : 0u;
+  uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
+  for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = tmp[i];
+  for (int i = threadIdx.x; i < cnt; i += NT) slot[kSlotListOff + i] = words[i];
+  if (threadIdx.x == 0)
+    slot[0] = static_cast<uint64_t>(cnt) | (static_cast<uint64_t>(lo) << 32) |
+              (static_cast<uint64_t>(nb) << 48);
+  __syncthreads();
+}
 
+// CTA-wide finish (split plans, and one-query CTAs whose selector warps keep separate pools):
+// for each query, the unused tails of its pools are zeroed (a CTA-wide select ignores zero
+// words), the 512 best words are radix-selected with all warps, and then either published
+// unordered as this split's list or sorted once and written as the output row.
 template <class C>
 __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split,
                                   uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
-                                  uint32_t* hist, uint32_t* scratch, int warp, int lane,
-                                  const float* sbuf, int buffered_keys, int64_t key0,
-                                  int64_t pos_b) {
+                                  uint32_t* hist, uint32_t* scratch, int warp, int lane) {
   constexpr int R = kTopK / 32;
   constexpr int kWords = C::kSelPerQuery * C::kPool;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
     if (t >= p.T) break;
-    int cnt;
-    if (buffered_keys > 0) {
-      const int64_t pt = pos_b + t;
-      const int64_t vis_end = (pt < p.S - 1 ? pt : p.S - 1) + 1;
-      constexpr int kStageWords = C::kStages * C::kKBytes / 8;
-      cnt = cta_select_sampled<kTopK, C::kThreads>(ScoreWords{sbuf, key0, vis_end}, buffered_keys,
-                                                   stage, stage + kTopK, kStageWords - kTopK,
-                                                   hist, scratch);
-    } else {
-      uint64_t* base = pools + q * kWords;
-      for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
-        const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
-        for (int i = used + threadIdx.x; i < C::kPool; i += C::kThreads)
-          base[sw * C::kPool + i] = 0ull;
-      }
-      __syncthreads();
-      cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
+    uint64_t* base = pools + q * kWords;
+    for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
+      const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
+      for (int i = used + threadIdx.x; i < C::kPool; i += C::kThreads) base[sw * C::kPool + i] = 0ull;
     }
+    __syncthreads();
+    const int cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
     const int64_t row = static_cast<int64_t>(b) * p.T + t;
     if (p.n_splits > 1) {
-      uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
-      for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
+      if constexpr (C::kHistSel) {
+        publish_slot<C::kThreads>(p.partial + (row * p.n_splits + split) * kSlotWords, stage, cnt,
+                                  hist, scratch, lane);
+      } else {
+        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
+        for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
+      }
     } else if (warp == 0) {
       uint64_t v[R];
 #pragma unroll
@@ -184,6 +248,341 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
     __syncthreads();
   }
   if (p.n_splits > 1) __threadfence();  // lists visible GPU-wide before the ticket is taken
+}
+
+// Writes the (up to) 512 best of the n distinct words ra.sv[0..n) as output row `row`, best
+// first. Every word's bin lies in [lo, hi], hi - lo < kRankBins. A counting sort by bin (best
+// bin first) gives each bin its range of positions; a word's final position is its bin's first
+// position plus the number of larger words in the same bin. Bins that start at or after
+// position 512 are not ranked.
+template <int NT>
+__device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, int n, uint32_t lo,
+                           uint32_t hi, int warp, int lane) {
+  const int range = static_cast<int>(hi - lo) + 1;
+  for (int i = threadIdx.x; i < range; i += NT) ra.cnt[i] = 0u;
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += NT) atomicAdd(&ra.cnt[hbin(ra.sv[i]) - lo], 1u);
+  __syncthreads();
+  if (warp == 0) {  // off[r] = words in bins above r, scanning down from the top bin
+    uint32_t acc = 0u;
+    for (int top = range - 1; top >= 0; top -= 32) {
+      const int r = top - lane;
+      const uint32_t c = r >= 0 ? ra.cnt[r] : 0u;
+      uint32_t s = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+      }
+      if (r >= 0) {
+        ra.off[r] = acc + s - c;
+        ra.cur[r] = acc + s - c;
+      }
+      acc += __shfl_sync(0xffffffffu, s, 31);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint64_t u = ra.sv[i];
+    ra.sorted[atomicAdd(&ra.cur[hbin(u) - lo], 1u)] = u;
+  }
+  __syncthreads();
+  int32_t* oi = p.out_idx + row * kTopK;
+  float* os = p.out_score ? p.out_score + row * kTopK : nullptr;
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint64_t u = ra.sorted[i];
+    const uint32_t r = hbin(u) - lo;
+    const int o = static_cast<int>(ra.off[r]);
+    if (o < kTopK) {
+      const int e = o + static_cast<int>(ra.cnt[r]);
+      int pos = o;
+#pragma unroll 4
+      for (int j = o; j < e; ++j) pos += ra.sorted[j] > u ? 1 : 0;
+      if (pos < kTopK) {
+        oi[pos] = key_index(u);
+        if (os) os[pos] = key_score(u);
+      }
+    }
+  }
+  for (int i = n + threadIdx.x; i < kTopK; i += NT) {
+    oi[i] = -1;
+    if (os) os[i] = -__int_as_float(0x7f800000);
+  }
+  __syncthreads();
+}
+
+// Buffered-mode words: the fp32 score of key key0 + i, packed, or 0 when the query cannot see it.
+struct ScoreWords {
+  const float* s;
+  int64_t key0, vis_end;
+  __device__ __forceinline__ uint64_t operator()(int i) const {
+    const int64_t key = key0 + i;
+    return key < vis_end ? pack_key(s[i], static_cast<uint32_t>(key)) : 0ull;
+  }
+};
+
+// Finish of a one-query CTA in buffered mode. During the stream the epilogue kept each key's
+// fp32 score (sbuf), a bit for every key whose bin reached the running cut bin at the time
+// (bits), and per-bin counts of those keys (bins). Counts at or above the final running cut are
+// exact, so one scan finds the exact bin b* of the 512th best word, and the keys with bin >= b*
+// (at least 512 of them unless fewer are visible, the CTA's 512 best among them) are read back
+// through the bitmap. A split publishes them with its count window; otherwise they are ranked
+// and written. Too many keys at b* (exact ties, a very flat score distribution) fall back to a
+// radix select over all buffered scores.
+template <class C>
+__device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint32_t* bins,
+                            const uint32_t* bits, const float* sbuf, int n_tiles, int64_t key0,
+                            int64_t vis_end, uint32_t floor_bin, uint32_t maxbin, uint64_t* stage,
+                            uint32_t* scratch, int warp, int lane) {
+  constexpr int NT = C::kThreads;
+  const int64_t row = static_cast<int64_t>(b) * p.T + t0;
+  if (warp == 0) {
+    uint32_t m;
+    const uint32_t bs = warp_find_cut<kTopK>(Hist16{bins}, floor_bin, maxbin, &m, lane);
+    if (lane == 0) {
+      scratch[0] = bs;
+      scratch[1] = m;
+      scratch[2] = 0u;
+    }
+  }
+  __syncthreads();
+  const uint32_t bstar = scratch[0];
+  const int m = static_cast<int>(scratch[1]);
+  const bool split_plan = p.n_splits > 1;
+  uint64_t* slot = split_plan ? p.partial + (row * p.n_splits + split) * kSlotWords : nullptr;
+  RankArea ra(reinterpret_cast<uint8_t*>(stage));
+  const bool fast = split_plan ? m <= kSlotListCap : (m <= kSurvCap && maxbin - bstar < kRankBins);
+  if (fast) {
+    uint64_t* dst = split_plan ? slot + kSlotListOff : ra.sv;
+    const uint32_t dst_cap = split_plan ? kSlotListCap : kSurvCap;  // never reached: m words match
+    const int nw = n_tiles * (kTileKeys / 32);
+    for (int w0 = 0; w0 < nw; w0 += NT) {  // one bitmap word (32 keys) per thread
+      const int wi = w0 + static_cast<int>(threadIdx.x);
+      const uint32_t bm = wi < nw ? bits[wi] : 0u;
+      uint32_t c = 0u;
+      for (uint32_t x = bm; x; x &= x - 1u) {
+        const int k = wi * 32 + __ffs(x) - 1;
+        c += hbin(pack_key(sbuf[k], static_cast<uint32_t>(key0 + k))) >= bstar ? 1u : 0u;
+      }
+      uint32_t s = c;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+      }
+      uint32_t at = 0u;
+      if (lane == 31 && s) at = atomicAdd(&scratch[2], s);
+      at = __shfl_sync(0xffffffffu, at, 31) + s - c;
+      for (uint32_t x = bm; x; x &= x - 1u) {
+        const int k = wi * 32 + __ffs(x) - 1;
+        const uint64_t u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
+        if (hbin(u) >= bstar && at < dst_cap) dst[at++] = u;
+      }
+    }
+    __syncthreads();
+    const int got = min(static_cast<int>(scratch[2]), static_cast<int>(dst_cap));
+    if (split_plan) {
+      const uint32_t lo =
+          maxbin - bstar >= static_cast<uint32_t>(kSlotHistBins) ? maxbin - (kSlotHistBins - 1) : bstar;
+      const uint32_t nb = got > 0 ? maxbin - lo + 1 : 0u;
+      uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
+      for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = Hist16{bins}(lo + i);
+      if (threadIdx.x == 0)
+        slot[0] = static_cast<uint64_t>(got) | (static_cast<uint64_t>(lo) << 32) |
+                  (static_cast<uint64_t>(nb) << 48);
+      __syncthreads();
+    } else {
+      rank_write<NT>(p, row, ra, got, bstar, maxbin, warp, lane);
+    }
+  } else {
+    constexpr int kStageWords = C::kStages * C::kKBytes / 8;
+    uint32_t* hist = bins;  // the counts are no longer needed
+    const int cnt = cta_select_sampled<kTopK, NT>(ScoreWords{sbuf, key0, vis_end},
+                                                  n_tiles * kTileKeys, stage, stage + kTopK,
+                                                  kStageWords - kTopK, hist, scratch);
+    if (split_plan) {
+      publish_slot<NT>(slot, stage, cnt, hist, scratch, lane);
+    } else {
+      constexpr int R = kTopK / 32;
+      if (warp == 0) {
+        uint64_t v[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) v[r] = lane * R + r < cnt ? stage[lane * R + r] : 0ull;
+        warp_sort_desc<R>(v, lane);
+        write_output<R>(p, row, v, lane);
+      }
+      __syncthreads();
+    }
+  }
+  if (split_plan) __threadfence();  // the slot is visible GPU-wide before the ticket is taken
+}
+
+// One-query split plans, part 2 (the CTA that takes the last ticket). The splits' count windows
+// are summed into one histogram, whose scan gives the highest bin G that at least 512 published
+// words reach; that bin holds or precedes the 512th best word overall. The lists are copied into
+// shared memory (in rounds when they do not fit at once) with independent 16-byte loads, the
+// words with bin >= G are kept and rank_write orders them. More survivors than the ranking takes
+// fall back to a radix select over all lists and one CTA-wide sort.
+template <class C>
+__device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* buf,
+                                 uint8_t* area, uint32_t* scratch, int warp, int lane) {
+  constexpr int NT = C::kThreads;
+  constexpr int kCap = C::kStages * C::kKBytes / 8;  // words of the gather area
+  constexpr int kPairs = kSlotListCap / 2;           // 16-byte pairs per list at most
+  constexpr int kUnroll = 8;
+  const RankArea ra(area);
+  uint32_t* mh = reinterpret_cast<uint32_t*>(ra.sv);  // kHBins counts; sv is written later
+  uint32_t* hm = ra.hdr;      // [64] list sizes
+  uint32_t* hlo = hm + 64;    // [64] window starts
+  uint32_t* hnb = hlo + 64;   // [64] window widths
+  uint32_t* hpre = hnb + 64;  // [65] list offsets in the gather area (sizes rounded up to even)
+  const int ns = p.n_splits;
+  const int64_t row = static_cast<int64_t>(b) * p.T + t0;
+  const uint64_t* slots = p.partial + row * ns * kSlotWords;
+  for (int i = threadIdx.x; i < ns; i += NT) {
+    const uint64_t h = slots[static_cast<int64_t>(i) * kSlotWords];
+    const uint32_t m = static_cast<uint32_t>(h);
+    const uint32_t lo = static_cast<uint32_t>(h >> 32) & 0xFFFFu;
+    const uint32_t nb = static_cast<uint32_t>(h >> 48);
+    hm[i] = m < static_cast<uint32_t>(kSlotListCap) ? m : static_cast<uint32_t>(kSlotListCap);
+    hlo[i] = lo;
+    hnb[i] = (nb <= static_cast<uint32_t>(kSlotHistBins) && lo + nb <= static_cast<uint32_t>(kHBins)) ? nb : 0u;
+  }
+  for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t acc = 0u, top = 0u;
+    for (int i0 = 0; i0 < ns; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t sz = i < ns ? (hm[i] + 1u) & ~1u : 0u;
+      if (i < ns && hnb[i]) top = max(top, hlo[i] + hnb[i] - 1u);
+      uint32_t s = sz;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+      }
+      if (i < ns) hpre[i] = acc + s - sz;
+      acc += __shfl_sync(0xffffffffu, s, 31);
+    }
+    top = __reduce_max_sync(0xffffffffu, top);
+    if (lane == 0) {
+      hpre[ns] = acc;
+      scratch[1] = top;
+    }
+  }
+  __syncthreads();
+  // Count windows into the histogram; meanwhile the first round of lists is copied in.
+  for (int j = threadIdx.x; j < ns * kSlotHistBins; j += NT) {
+    const int i = j / kSlotHistBins, k = j - i * kSlotHistBins;
+    if (k < static_cast<int>(hnb[i])) {
+      const uint32_t c = reinterpret_cast<const uint32_t*>(
+          slots + static_cast<int64_t>(i) * kSlotWords + kSlotHdrWords)[k];
+      if (c) atomicAdd(&mh[hlo[i] + k], c);
+    }
+  }
+  auto round_end = [&](int i0) {
+    int i1 = i0 + 1;
+    while (i1 < ns && hpre[i1 + 1] - hpre[i0] <= static_cast<uint32_t>(kCap)) ++i1;
+    return i1;
+  };
+  auto copy_round = [&](int i0, int i1) {
+    const uint32_t base = hpre[i0];
+    const int np = (i1 - i0) * kPairs;
+    for (int g0 = 0; g0 < np; g0 += kUnroll * NT) {
+      uint4 v[kUnroll];
+      int d[kUnroll];
+#pragma unroll
+      for (int r = 0; r < kUnroll; ++r) {
+        const int g = g0 + r * NT + static_cast<int>(threadIdx.x);
+        d[r] = -1;
+        v[r] = make_uint4(0u, 0u, 0u, 0u);
+        if (g < np) {
+          const int li = g / kPairs;
+          const int j = g - li * kPairs;
+          const int i = i0 + li;
+          const int m = static_cast<int>(hm[i]);
+          if (2 * j < m) {
+            v[r] = *reinterpret_cast<const uint4*>(slots + static_cast<int64_t>(i) * kSlotWords +
+                                                   kSlotListOff + 2 * j);
+            if (2 * j + 1 == m) v[r].z = v[r].w = 0u;  // odd list: zero its padding word
+            d[r] = static_cast<int>(hpre[i] - base) + 2 * j;
+          }
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < kUnroll; ++r)
+        if (d[r] >= 0) *reinterpret_cast<uint4*>(buf + d[r]) = v[r];
+    }
+  };
+  int i0 = 0;
+  int i1 = ns > 0 ? round_end(0) : 0;
+  if (ns > 0) copy_round(0, i1);
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t c;
+    const uint32_t g = warp_find_cut<kTopK>(Hist32{mh}, 0u, scratch[1], &c, lane);
+    if (lane == 0) {
+      scratch[0] = g;
+      scratch[2] = 0u;
+    }
+  }
+  __syncthreads();
+  const uint32_t G = scratch[0], H = scratch[1];
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  while (i0 < ns) {
+    const int nw = static_cast<int>(hpre[i1] - hpre[i0]);
+    for (int x0 = 0; x0 < nw; x0 += NT) {
+      const int x = x0 + static_cast<int>(threadIdx.x);
+      const uint64_t u = x < nw ? buf[x] : 0ull;
+      const uint32_t bn = hbin(u);
+      const bool keep = u != 0ull && bn >= G && bn <= H;  // every published bin is <= H
+      const uint32_t km = __ballot_sync(0xffffffffu, keep);
+      uint32_t at = 0u;
+      if (lane == 0 && km) at = atomicAdd(&scratch[2], __popc(km));
+      at = __shfl_sync(0xffffffffu, at, 0) + __popc(km & lt_mask);
+      if (keep && at < static_cast<uint32_t>(kSurvCap)) ra.sv[at] = u;
+    }
+    __syncthreads();
+    i0 = i1;
+    if (i0 < ns) {
+      i1 = round_end(i0);
+      copy_round(i0, i1);
+      __syncthreads();
+    }
+  }
+  const int n_sv = static_cast<int>(scratch[2]);
+  __syncthreads();
+  if (n_sv <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins)) {
+    rank_write<NT>(p, row, ra, n_sv, G, H, warp, lane);
+    return;
+  }
+  // Rare: too many published words at the cut bin. Exact radix selection over every list,
+  // folded whenever the gather area would overflow, then one CTA-wide sort.
+  uint64_t* sel = ra.sorted;
+  int n = 0;
+  for (int i = 0; i < ns; ++i) {
+    if (n + kSlotListCap > kCap) {
+      const int k = cta_select<kTopK, NT>(buf, n, sel, ra.rhist, scratch);
+      for (int x = threadIdx.x; x < k; x += NT) buf[x] = sel[x];
+      __syncthreads();
+      n = k;
+    }
+    const uint64_t* src = slots + static_cast<int64_t>(i) * kSlotWords + kSlotListOff;
+    for (int x = threadIdx.x; x < static_cast<int>(hm[i]); x += NT) buf[n + x] = src[x];
+    __syncthreads();
+    n += static_cast<int>(hm[i]);
+  }
+  const int cnt = cta_select<kTopK, NT>(buf, n, sel, ra.rhist, scratch);
+  for (int x = cnt + threadIdx.x; x < kTopK; x += NT) sel[x] = 0ull;
+  __syncthreads();
+  cta_sort_desc<kTopK, NT>(sel);
+  for (int i = threadIdx.x; i < kTopK; i += NT) {
+    const uint64_t u = sel[i];
+    p.out_idx[row * kTopK + i] = u ? key_index(u) : -1;
+    if (p.out_score) p.out_score[row * kTopK + i] = u ? key_score(u) : -__int_as_float(0x7f800000);
+  }
+  __syncthreads();
 }
 
 // Split plans, part 2 (the CTA that takes a block's last ticket): copy every split's list of
@@ -248,7 +647,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint8_t* sK = smem + C::kOffK;
   float* sW = reinterpret_cast<float*>(smem + C::kOffW);
   float* sScore = reinterpret_cast<float*>(smem + C::kOffRing);
-  float* sBuf = reinterpret_cast<float*>(smem + C::kOffRing);  // buffered mode only
+  // buffered mode only: scores, candidate bitmap, per-bin counts
+  float* sBuf = reinterpret_cast<float*>(smem + C::kOffBuf);
+  uint32_t* s_bits = reinterpret_cast<uint32_t*>(smem + C::kOffBits);
+  uint32_t* s_bins = reinterpret_cast<uint32_t*>(smem + C::kOffBins);
   uint64_t* sPool = reinterpret_cast<uint64_t*>(smem + C::kOffPool);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -267,6 +669,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   // Running threshold published by each selector warp (only rises): a query's warps filter
   // against the largest of them, which is still at most the CTA's exact 512th best.
   volatile uint64_t* s_theta = reinterpret_cast<volatile uint64_t*>(smem + C::kOffMisc + 64);
+  // Buffered mode: running cut bin (only rises), candidates so far, highest candidate bin.
+  uint32_t* s_cut = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 96);
+  uint32_t* s_cand = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 100);
+  uint32_t* s_maxbin = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 104);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -295,6 +701,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   }
 
   const bool buffered = C::kBufTiles > 0 && n_tiles <= C::kBufTiles;
+  // Keys a one-query CTA's query can see: [0, vis_q).
+  const int64_t vis_q = (pos_b + t0 < p.S - 1 ? pos_b + t0 : p.S - 1) + 1;
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -313,8 +721,13 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     mbar_init(qfull, 1);
     *s_abort = 0u;
     for (int i = 0; i < C::kSelectors; ++i) s_theta[i] = 0ull;
+    *s_cut = 0u;
+    *s_cand = 0u;
+    *s_maxbin = 0u;
     fence_mbar_init();
   }
+  if (buffered)
+    for (int i = threadIdx.x; i < C::kBinsBytes / 4; i += C::kThreads) s_bins[i] = 0u;
   if (warp == C::kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tmap_q);
     tma_prefetch_desc(&tmap_k);
@@ -475,6 +888,37 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
             }
           } else if (buffered) {
             sBuf[it * kTileKeys + quad * 32 + lane] = score;
+            // Running cut: a key is a candidate when its bin reaches the cut bin, which some
+            // 512 candidates already reach (so it never exceeds the bin of the CTA's 512th
+            // best). Candidates are marked in the bitmap and counted per bin; every kRecut
+            // candidates the warp that crosses the mark raises the cut from the counts.
+            const uint64_t u = key < vis_q ? pack_key(score, static_cast<uint32_t>(key)) : 0ull;
+            const uint32_t bn = hbin(u);
+            const bool keep = u != 0ull && bn >= *reinterpret_cast<volatile uint32_t*>(s_cut);
+            const uint32_t km = __ballot_sync(0xffffffffu, keep);
+            if (lane == 0) s_bits[it * (kTileKeys / 32) + quad] = km;
+            if (km) {
+              if (keep) hist16_inc(s_bins, bn);
+              const uint32_t mb = __reduce_max_sync(0xffffffffu, keep ? bn : 0u);
+              uint32_t before = 0u;
+              if (lane == 0) {
+                atomicMax(s_maxbin, mb);
+                before = atomicAdd(s_cand, static_cast<uint32_t>(__popc(km)));
+              }
+              before = __shfl_sync(0xffffffffu, before, 0);
+              if ((before + __popc(km)) / kRecut != before / kRecut) {
+                __syncwarp();
+                uint32_t lo = 0u, hi = 0u, cnt;
+                if (lane == 0) {
+                  lo = *reinterpret_cast<volatile uint32_t*>(s_cut);
+                  hi = *reinterpret_cast<volatile uint32_t*>(s_maxbin);
+                }
+                lo = __shfl_sync(0xffffffffu, lo, 0);
+                hi = __shfl_sync(0xffffffffu, hi, 0);
+                const uint32_t nb = warp_find_cut<kTopK>(Hist16{s_bins}, lo, hi, &cnt, lane);
+                if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK)) atomicMax(s_cut, nb);
+              }
+            }
           } else {
             sScore[(sb * NQ + q) * kTileKeys + quad * 32 + lane] = score;
           }
@@ -559,10 +1003,15 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
   }
-  if (!DENSE && (C::kSelPerQuery > 1 || p.n_splits > 1) && !*s_abort)
-    finish_cta_select<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK), sHist,
-                         s_scratch, warp, lane, sBuf, buffered ? n_tiles * kTileKeys : 0,
-                         static_cast<int64_t>(tile_lo) * kTileKeys, pos_b);
+  if (!DENSE && !*s_abort) {
+    if (buffered)
+      finish_hist<C>(p, b, t0, split, s_bins, s_bits, sBuf, n_tiles,
+                     static_cast<int64_t>(tile_lo) * kTileKeys, vis_q, *s_cut, *s_maxbin,
+                     reinterpret_cast<uint64_t*>(sK), s_scratch, warp, lane);
+    else if (C::kSelPerQuery > 1 || p.n_splits > 1)
+      finish_cta_select<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK),
+                           sHist, s_scratch, warp, lane);
+  }
   if (!DENSE && p.n_splits > 1) {
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
@@ -574,9 +1023,14 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     __syncthreads();
     if (*s_last) {
       __threadfence();
-      if (!*s_abort)
-        merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch, warp,
-                             lane);
+      if (!*s_abort) {
+        if constexpr (C::kHistSel)
+          merge_hist_slots<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), smem + C::kOffHist,
+                              s_scratch, warp, lane);
+        else
+          merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch, warp,
+                               lane);
+      }
       if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
     }
   }

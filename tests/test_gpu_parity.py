@@ -206,3 +206,65 @@ def test_split_merge_concentrated_winners(fp8_ix, bf16_ix):
         stats, gi, _ = run_full(prob, ix)
         hits = np.sum((gi[0] >= 12000) & (gi[0] < 12400))
         assert hits > 300, hits  # the winners really are concentrated
+
+
+# ---- one-query CTAs: running cut bin, candidate bitmap, bin-ranked finish and slot merge
+
+@pytest.mark.parametrize("S", [1, 100, 511, 512, 513, 700, 896])
+def test_single_query_unsplit(S, bf16_ix, fp8_ix):
+    # Up to 7 key tiles: one CTA, no split; the CTA ranks its candidates by bin itself and pads
+    # rows that see fewer than 512 keys.
+    for dtype, ix in ((inputs.BF16, bf16_ix), (inputs.FP8_E4M3, fp8_ix)):
+        prob = inputs.make("q1", T=1, S=S, pos_offset=S - 1, seed=40 + S, dtype=dtype)
+        stats, gi, gs = run_full(prob, ix)
+        n = min(S, 512)
+        assert np.all(gi[0, n:] == -1)
+        if S <= 512:
+            assert sorted(gi[0, :n].tolist()) == list(range(n))
+
+
+@pytest.mark.parametrize("S", [5000, 30000])
+def test_single_query_tie_storm(S, bf16_ix):
+    # Every score is exactly 0 (one bin): the splits publish every tied key (S = 5000) or fall
+    # back to an exact select (S = 30000), and the merge falls back to the radix path.
+    prob = inputs.make("ties1", T=1, S=S, pos_offset=S - 1, seed=50, dtype=inputs.BF16)
+    prob.k.zero_()
+    stats, gi, gs = run_full(prob, bf16_ix)
+    assert gi[0].tolist() == list(range(512))
+    assert np.all(gs[0] == 0.0)
+
+
+def test_single_query_all_negative(bf16_ix):
+    prob = inputs.make("neg1", T=1, S=20000, pos_offset=19999, seed=51, dtype=inputs.BF16)
+    prob.w.copy_(-prob.w.abs())
+    stats, _, gs = run_full(prob, bf16_ix)
+    assert np.all(gs[0] <= 0.0)
+
+
+def test_single_query_wide_dynamic_range(fp8_ix):
+    # A few keys scaled by 1e3 and 1e6 put the top bins hundreds of bins above the cut: the
+    # published count windows are clipped to their top 256 bins (an undercount the merge allows).
+    prob = inputs.make("wide1", T=1, S=30000, pos_offset=29999, seed=52, dtype=inputs.FP8_E4M3)
+    g = torch.Generator().manual_seed(52)
+    pick = torch.randperm(30000, generator=g)[:100]
+    prob.kscale[pick[:50]] *= 1e6
+    prob.kscale[pick[50:]] *= 1e3
+    run_full(prob, fp8_ix)
+
+
+def test_single_query_batched_splits_deterministic(fp8_ix):
+    probs = [inputs.make(f"d{b}", T=1, S=40000, pos_offset=39999 - 977 * b, seed=60 + b,
+                         dtype=inputs.FP8_E4M3) for b in range(8)]
+    q = torch.stack([p.q for p in probs]).cuda()
+    w = torch.stack([p.w for p in probs]).cuda()
+    k = torch.stack([p.k for p in probs]).cuda()
+    ks = torch.stack([p.kscale for p in probs]).cuda()
+    pos = [p.pos_offset for p in probs]
+    idx, sc = fp8_ix.score_topk_batched(q, w, k, ks, pos)
+    fp8_ix.sync_status()
+    for _ in range(3):
+        idx2, sc2 = fp8_ix.score_topk_batched(q, w, k, ks, pos)
+        fp8_ix.sync_status()
+        assert torch.equal(idx, idx2) and torch.equal(sc, sc2)
+    for b, prob in enumerate(probs):
+        parity.check_rows(prob, [0], idx[b].cpu().numpy(), sc[b].cpu().numpy())
