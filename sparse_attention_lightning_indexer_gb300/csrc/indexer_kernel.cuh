@@ -54,8 +54,8 @@ constexpr int kSlotListOff = kSlotHdrWords + kSlotHistBins / 2;
 constexpr int kSlotWords = 1152;
 constexpr int kSlotListCap = kSlotWords - kSlotListOff;
 constexpr int kSurvCap = 2048;   // words the bin-ranked final selection takes at most
-constexpr int kRankBins = 1024;  // bins it spans at most
-constexpr int kRecut = 256;      // new candidates between two raises of the epilogue's cut bin
+constexpr int kRankBins = 2048;  // bins (and refined buckets) it spans at most
+constexpr int kRecut = 64;       // a warp's own candidates between its raises of the cut bin
 
 // Shared-memory scratch of the bin-ranked final selection and of the slot merge.
 struct RankArea {
@@ -99,7 +99,7 @@ struct KCfg {
   static constexpr int kN = kHeads * NQ;                             // MMA N
   static constexpr int kQBytes = kN * kRowBytes;
   static constexpr int kKBytes = kTileKeys * kRowBytes;
-  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 5) : (NQ == 4 ? 6 : 8);
+  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 4) : (NQ == 4 ? 6 : 8);
   static constexpr int kKSteps = DT == kDtBf16 ? kDim / 16 : kDim / 32;
   static constexpr int kStepBytes = 32;                              // K bytes per MMA step
   // Depth of the epilogue -> selector score ring: it lets selectors fall behind by that many
@@ -138,22 +138,25 @@ struct KCfg {
   static constexpr int kOffRing = kOffHist + (DENSE ? 0 : kSelectors * 256 * 4);
   static constexpr int kOffPool = kOffRing + (DENSE ? 0 : kScoreBufs * NQ * kTileKeys * 4);
   static constexpr int kOffSelEnd = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
-  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 1;
-  static constexpr int kMiscBytes = 128;
+  static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 2;
+  static constexpr int kMiscBytes = 160;
   // Buffered selection (one-query CTAs whose key split fits): the epilogue keeps every fp32
-  // score of the split, a bitmap of the keys that beat its running cut bin, and 16-bit per-bin
-  // counts of those keys; the final selection reads them back (finish_hist). These overlay the
-  // selector histograms, the ring and the pools, which that mode leaves unused, plus whatever
-  // shared memory is left.
+  // score of the split, counts the keys that reach a running cut bin per bin (16-bit counters)
+  // and lists their offsets (one list per epilogue warp), while a selector warp raises the cut;
+  // the final selection reads them back (finish_hist). These overlay the selector histograms,
+  // the ring and the pools, which that mode leaves unused, plus whatever shared memory is left.
   static constexpr bool kHistSel = NQ == 1 && !DENSE;
-  static constexpr int kBinsBytes = kHBins * 2;
+  static constexpr int kBinsBytes = kHBins * 2 + (kHBins / 32) * 4;  // bins, then 32-bin groups
+  static constexpr int kCandSeg = 512;  // candidate offsets per epilogue warp (16-bit)
+  static constexpr int kCandBytes = kHistSel ? kEpiWarps * kCandSeg * 2 : 0;
   static constexpr int kBufTiles =
-      kHistSel ? (232448 - 1024 - kMiscBytes - kNumBars * 8 - kOffHist - kBinsBytes) /
-                     (kTileKeys * 4 + 16)
+      kHistSel ? (232448 - 1024 - kMiscBytes - kNumBars * 8 - kOffHist - kBinsBytes - kCandBytes) /
+                     (kTileKeys * 4)
                : 0;
+  static_assert(kBufTiles * kTileKeys <= 65536, "16-bit candidate offsets");
   static constexpr int kOffBins = kOffHist;
-  static constexpr int kOffBits = kOffBins + kBinsBytes;
-  static constexpr int kOffBuf = kOffBits + kBufTiles * 16;
+  static constexpr int kOffCand = kOffBins + kBinsBytes;
+  static constexpr int kOffBuf = kOffCand + kCandBytes;
   static constexpr int kBufEnd = kHistSel ? kOffBuf + kBufTiles * kTileKeys * 4 : 0;
   static constexpr int kOffBar = kOffSelEnd > kBufEnd ? kOffSelEnd : kBufEnd;
   static_assert(!kHistSel || kOffBar - kOffHist >= RankArea::kBytes, "slot merge area");
@@ -247,57 +250,71 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
     }
     __syncthreads();
   }
-  if (p.n_splits > 1) __threadfence();  // lists visible GPU-wide before the ticket is taken
+  if (p.n_splits > 1) {  // lists visible GPU-wide (also to bulk copies) before the ticket
+    fence_proxy_async_global();
+    __threadfence();
+  }
 }
 
 // Writes the (up to) 512 best of the n distinct words ra.sv[0..n) as output row `row`, best
-// first. Every word's bin lies in [lo, hi], hi - lo < kRankBins. A counting sort by bin (best
-// bin first) gives each bin its range of positions; a word's final position is its bin's first
-// position plus the number of larger words in the same bin. Bins that start at or after
+// first. Every word's bin lies in [lo, hi], hi - lo < kRankBins. Words are bucketed by their
+// bin refined with e more bits of the code (e as large as kRankBins buckets allow), a counting
+// sort over the buckets (best first, CTA-wide suffix scan) gives each bucket its range of
+// positions, and a word's final position is its bucket's first position plus the number of
+// larger words in the same bucket (buckets hold a few words). Buckets that start at or after
 // position 512 are not ranked.
 template <int NT>
 __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, int n, uint32_t lo,
                            uint32_t hi, int warp, int lane) {
-  const int range = static_cast<int>(hi - lo) + 1;
+  constexpr int kWarps = NT / 32;
+  int e = 0;
+  while (e < 20 && ((static_cast<int>(hi - lo) + 1) << (e + 1)) <= kRankBins) ++e;
+  const int range = (static_cast<int>(hi - lo) + 1) << e;
+  const int shift = 52 - e;
+  const uint64_t base = static_cast<uint64_t>(lo) << e;
+  auto bucket = [&](uint64_t u) { return static_cast<int>((u >> shift) - base); };
   for (int i = threadIdx.x; i < range; i += NT) ra.cnt[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += NT) atomicAdd(&ra.cnt[hbin(ra.sv[i]) - lo], 1u);
+  for (int i = threadIdx.x; i < n; i += NT) atomicAdd(&ra.cnt[bucket(ra.sv[i])], 1u);
   __syncthreads();
-  if (warp == 0) {  // off[r] = words in bins above r, scanning down from the top bin
-    uint32_t acc = 0u;
-    for (int top = range - 1; top >= 0; top -= 32) {
-      const int r = top - lane;
-      const uint32_t c = r >= 0 ? ra.cnt[r] : 0u;
-      uint32_t s = c;
+  // off[r] = words in buckets above r. Thread t owns the buckets v = t*per .. t*per+per-1 counted
+  // from the top (r = range-1-v); a block-wide exclusive prefix of the per-thread sums follows.
+  const int per = (range + NT - 1) / NT;
+  const int v0 = static_cast<int>(threadIdx.x) * per;
+  uint32_t own = 0u;
+  for (int v = v0; v < v0 + per && v < range; ++v) own += ra.cnt[range - 1 - v];
+  uint32_t s = own;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += v;
-      }
-      if (r >= 0) {
-        ra.off[r] = acc + s - c;
-        ra.cur[r] = acc + s - c;
-      }
-      acc += __shfl_sync(0xffffffffu, s, 31);
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += x;
+  }
+  if (lane == 31) ra.rhist[warp] = s;
+  __syncthreads();
+  uint32_t run = s - own;
+  for (int w = 0; w < warp; ++w) run += ra.rhist[w];
+  for (int v = v0; v < v0 + per && v < range; ++v) {
+    const int r = range - 1 - v;
+    ra.off[r] = run;
+    ra.cur[r] = run;
+    run += ra.cnt[r];
   }
   __syncthreads();
   for (int i = threadIdx.x; i < n; i += NT) {
     const uint64_t u = ra.sv[i];
-    ra.sorted[atomicAdd(&ra.cur[hbin(u) - lo], 1u)] = u;
+    ra.sorted[atomicAdd(&ra.cur[bucket(u)], 1u)] = u;
   }
   __syncthreads();
   int32_t* oi = p.out_idx + row * kTopK;
   float* os = p.out_score ? p.out_score + row * kTopK : nullptr;
   for (int i = threadIdx.x; i < n; i += NT) {
     const uint64_t u = ra.sorted[i];
-    const uint32_t r = hbin(u) - lo;
+    const int r = bucket(u);
     const int o = static_cast<int>(ra.off[r]);
     if (o < kTopK) {
-      const int e = o + static_cast<int>(ra.cnt[r]);
+      const int end = o + static_cast<int>(ra.cnt[r]);
       int pos = o;
-#pragma unroll 4
-      for (int j = o; j < e; ++j) pos += ra.sorted[j] > u ? 1 : 0;
+      for (int j = o; j < end; ++j) pos += ra.sorted[j] > u ? 1 : 0;
       if (pos < kTopK) {
         oi[pos] = key_index(u);
         if (os) os[pos] = key_score(u);
@@ -308,6 +325,7 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
     oi[i] = -1;
     if (os) os[i] = -__int_as_float(0x7f800000);
   }
+  static_assert(kWarps <= 256, "per-warp sums fit the radix scratch");
   __syncthreads();
 }
 
@@ -322,73 +340,93 @@ struct ScoreWords {
 };
 
 // Finish of a one-query CTA in buffered mode. During the stream the epilogue kept each key's
-// fp32 score (sbuf), a bit for every key whose bin reached the running cut bin at the time
-// (bits), and per-bin counts of those keys (bins). Counts at or above the final running cut are
-// exact, so one scan finds the exact bin b* of the 512th best word, and the keys with bin >= b*
-// (at least 512 of them unless fewer are visible, the CTA's 512 best among them) are read back
-// through the bitmap. A split publishes them with its count window; otherwise they are ranked
-// and written. Too many keys at b* (exact ties, a very flat score distribution) fall back to a
-// radix select over all buffered scores.
+// fp32 score (sbuf) and listed, per epilogue warp, the offsets of the keys whose bin reached
+// the running cut bin at the time (cand, ncand) and counted them per bin (bins). Counts
+// at or above the final running cut are exact, so one scan finds the exact bin b* of the 512th
+// best word, and the listed keys with bin >= b* (at least 512 of them unless fewer are visible,
+// the CTA's 512 best among them) are read back. A split publishes them with its count window;
+// otherwise they are ranked and written. A full candidate list, or too many keys at b* (exact
+// ties, a very flat score distribution), fall back to a radix select over all buffered scores.
 template <class C>
 __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint32_t* bins,
-                            const uint32_t* bits, const float* sbuf, int n_tiles, int64_t key0,
-                            int64_t vis_end, uint32_t floor_bin, uint32_t maxbin, uint64_t* stage,
-                            uint32_t* scratch, int warp, int lane) {
+                            const uint16_t* cand, const uint32_t* ncand, const float* sbuf,
+                            int n_tiles, int64_t key0, int64_t vis_end, uint32_t floor_bin,
+                            uint32_t maxbin, uint64_t* stage, uint32_t* scratch, int warp,
+                            int lane) {
   constexpr int NT = C::kThreads;
+  constexpr int kWarps = NT / 32;
+  constexpr int kSegs = C::kEpiWarps;
   const int64_t row = static_cast<int64_t>(b) * p.T + t0;
   if (warp == 0) {
     uint32_t m;
-    const uint32_t bs = warp_find_cut<kTopK>(Hist16{bins}, floor_bin, maxbin, &m, lane);
+    const uint32_t bs =
+        warp_find_cut_grouped<kTopK>(bins, bins + kHBins / 2, floor_bin, maxbin, &m, lane);
     if (lane == 0) {
       scratch[0] = bs;
       scratch[1] = m;
-      scratch[2] = 0u;
     }
   }
   __syncthreads();
   const uint32_t bstar = scratch[0];
   const int m = static_cast<int>(scratch[1]);
+  bool listed = true;
+#pragma unroll
+  for (int s = 0; s < kSegs; ++s) listed = listed && ncand[s] <= static_cast<uint32_t>(C::kCandSeg);
   const bool split_plan = p.n_splits > 1;
   uint64_t* slot = split_plan ? p.partial + (row * p.n_splits + split) * kSlotWords : nullptr;
   RankArea ra(reinterpret_cast<uint8_t*>(stage));
-  const bool fast = split_plan ? m <= kSlotListCap : (m <= kSurvCap && maxbin - bstar < kRankBins);
+  const bool fast = listed && (split_plan ? m <= kSlotListCap
+                                          : (m <= kSurvCap && maxbin - bstar < kRankBins));
   if (fast) {
     uint64_t* dst = split_plan ? slot + kSlotListOff : ra.sv;
     const uint32_t dst_cap = split_plan ? kSlotListCap : kSurvCap;  // never reached: m words match
-    const int nw = n_tiles * (kTileKeys / 32);
-    for (int w0 = 0; w0 < nw; w0 += NT) {  // one bitmap word (32 keys) per thread
-      const int wi = w0 + static_cast<int>(threadIdx.x);
-      const uint32_t bm = wi < nw ? bits[wi] : 0u;
-      uint32_t c = 0u;
-      for (uint32_t x = bm; x; x &= x - 1u) {
-        const int k = wi * 32 + __ffs(x) - 1;
-        c += hbin(pack_key(sbuf[k], static_cast<uint32_t>(key0 + k))) >= bstar ? 1u : 0u;
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    // The lists side by side: position i is entry i % kCandSeg of list i / kCandSeg. Two passes
+    // over a stripe per warp (count, then write at the warp's offset), no shared atomics.
+    constexpr int kSpan = kSegs * C::kCandSeg;
+    constexpr int kPerWarp = (kSpan + kWarps - 1) / kWarps;
+    const int lo = warp * kPerWarp, hi = lo + kPerWarp < kSpan ? lo + kPerWarp : kSpan;
+    auto word_at = [&](int i, uint32_t& km) -> uint64_t {
+      uint64_t u = 0ull;
+      if (i < hi) {
+        const int s = i / C::kCandSeg;
+        if (static_cast<uint32_t>(i - s * C::kCandSeg) < ncand[s]) {
+          const int k = cand[i];
+          u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
+        }
       }
-      uint32_t s = c;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += v;
-      }
-      uint32_t at = 0u;
-      if (lane == 31 && s) at = atomicAdd(&scratch[2], s);
-      at = __shfl_sync(0xffffffffu, at, 31) + s - c;
-      for (uint32_t x = bm; x; x &= x - 1u) {
-        const int k = wi * 32 + __ffs(x) - 1;
-        const uint64_t u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
-        if (hbin(u) >= bstar && at < dst_cap) dst[at++] = u;
-      }
+      km = __ballot_sync(0xffffffffu, u != 0ull && hbin(u) >= bstar);
+      return u;
+    };
+    uint32_t cnt = 0u;
+    for (int x = lo; x < hi; x += 32) {
+      uint32_t km;
+      word_at(x + lane, km);
+      cnt += __popc(km);
+    }
+    uint32_t* wcnt = ra.rhist;  // not part of sv
+    if (lane == 0) wcnt[warp] = cnt;
+    __syncthreads();
+    uint32_t at = 0u;
+    for (int w = 0; w < warp; ++w) at += wcnt[w];
+    if (warp == kWarps - 1 && lane == 0) scratch[2] = at + cnt;
+    for (int x = lo; x < hi; x += 32) {
+      uint32_t km;
+      const uint64_t u = word_at(x + lane, km);
+      const uint32_t pos = at + __popc(km & lt_mask);
+      if ((km >> lane) & 1u && pos < dst_cap) dst[pos] = u;
+      at += __popc(km);
     }
     __syncthreads();
     const int got = min(static_cast<int>(scratch[2]), static_cast<int>(dst_cap));
     if (split_plan) {
-      const uint32_t lo =
+      const uint32_t wlo =
           maxbin - bstar >= static_cast<uint32_t>(kSlotHistBins) ? maxbin - (kSlotHistBins - 1) : bstar;
-      const uint32_t nb = got > 0 ? maxbin - lo + 1 : 0u;
+      const uint32_t nb = got > 0 ? maxbin - wlo + 1 : 0u;
       uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
-      for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = Hist16{bins}(lo + i);
+      for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = Hist16{bins}(wlo + i);
       if (threadIdx.x == 0)
-        slot[0] = static_cast<uint64_t>(got) | (static_cast<uint64_t>(lo) << 32) |
+        slot[0] = static_cast<uint64_t>(got) | (static_cast<uint64_t>(wlo) << 32) |
                   (static_cast<uint64_t>(nb) << 48);
       __syncthreads();
     } else {
@@ -414,28 +452,32 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
       __syncthreads();
     }
   }
-  if (split_plan) __threadfence();  // the slot is visible GPU-wide before the ticket is taken
+  if (split_plan) {  // the slot is visible GPU-wide (also to bulk copies) before the ticket
+    fence_proxy_async_global();
+    __threadfence();
+  }
 }
 
 // One-query split plans, part 2 (the CTA that takes the last ticket). The splits' count windows
 // are summed into one histogram, whose scan gives the highest bin G that at least 512 published
-// words reach; that bin holds or precedes the 512th best word overall. The lists are copied into
-// shared memory (in rounds when they do not fit at once) with independent 16-byte loads, the
-// words with bin >= G are kept and rank_write orders them. More survivors than the ranking takes
-// fall back to a radix select over all lists and one CTA-wide sort.
+// words reach; the 512th best word overall lies in G or above. The lists are brought into
+// shared memory by bulk copies (in rounds when they do not fit at once; one round trip each),
+// the words with bin >= G are compacted and rank_write orders them. More survivors than the
+// ranking takes fall back to a radix select over all lists and one CTA-wide sort.
 template <class C>
 __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* buf,
-                                 uint8_t* area, uint32_t* scratch, int warp, int lane) {
+                                 uint8_t* area, uint64_t* gbar, volatile uint32_t* abort_flag,
+                                 uint32_t* scratch, int warp, int lane) {
   constexpr int NT = C::kThreads;
+  constexpr int kWarps = NT / 32;
   constexpr int kCap = C::kStages * C::kKBytes / 8;  // words of the gather area
-  constexpr int kPairs = kSlotListCap / 2;           // 16-byte pairs per list at most
-  constexpr int kUnroll = 8;
   const RankArea ra(area);
   uint32_t* mh = reinterpret_cast<uint32_t*>(ra.sv);  // kHBins counts; sv is written later
   uint32_t* hm = ra.hdr;      // [64] list sizes
   uint32_t* hlo = hm + 64;    // [64] window starts
   uint32_t* hnb = hlo + 64;   // [64] window widths
   uint32_t* hpre = hnb + 64;  // [65] list offsets in the gather area (sizes rounded up to even)
+  uint32_t* wcnt = ra.rhist;  // [kWarps] survivors per warp
   const int ns = p.n_splits;
   const int64_t row = static_cast<int64_t>(b) * p.T + t0;
   const uint64_t* slots = p.partial + row * ns * kSlotWords;
@@ -449,13 +491,17 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
     hnb[i] = (nb <= static_cast<uint32_t>(kSlotHistBins) && lo + nb <= static_cast<uint32_t>(kHBins)) ? nb : 0u;
   }
   for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
+  fence_proxy_async_smem();  // earlier generic accesses to the gather area precede the copies
   __syncthreads();
   if (warp == 0) {
-    uint32_t acc = 0u, top = 0u;
+    uint32_t acc = 0u, top = 0u, bottom = kHBins - 1;
     for (int i0 = 0; i0 < ns; i0 += 32) {
       const int i = i0 + lane;
       const uint32_t sz = i < ns ? (hm[i] + 1u) & ~1u : 0u;
-      if (i < ns && hnb[i]) top = max(top, hlo[i] + hnb[i] - 1u);
+      if (i < ns && hnb[i]) {
+        top = max(top, hlo[i] + hnb[i] - 1u);
+        bottom = min(bottom, hlo[i]);
+      }
       uint32_t s = sz;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -466,13 +512,41 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
       acc += __shfl_sync(0xffffffffu, s, 31);
     }
     top = __reduce_max_sync(0xffffffffu, top);
+    bottom = __reduce_min_sync(0xffffffffu, bottom);
     if (lane == 0) {
       hpre[ns] = acc;
       scratch[1] = top;
+      scratch[2] = 0u;
+      scratch[3] = bottom < top ? bottom : top;  // lowest counted bin
     }
   }
   __syncthreads();
-  // Count windows into the histogram; meanwhile the first round of lists is copied in.
+  auto round_end = [&](int i0) {
+    int i1 = i0 + 1;
+    while (i1 < ns && hpre[i1 + 1] - hpre[i0] <= static_cast<uint32_t>(kCap)) ++i1;
+    return i1;
+  };
+  // One warp arms the barrier with the round's bytes, then its lanes issue a copy per list.
+  auto issue_round = [&](int i0, int i1) {
+    const uint32_t base = hpre[i0];
+    uint32_t bytes = 0u;
+    for (int i = i0 + lane; i < i1; i += 32) bytes += ((hm[i] + 1u) / 2u) * 16u;
+    bytes = __reduce_add_sync(0xffffffffu, bytes);
+    if (lane == 0) mbar_arrive_expect_tx(gbar, bytes);
+    __syncwarp();
+    fence_proxy_async_global();  // the lists published by other CTAs, seen by the copies
+    for (int i = i0 + lane; i < i1; i += 32) {
+      const uint32_t m = hm[i];
+      if (m)
+        bulk_load(buf + (hpre[i] - base),
+                  slots + static_cast<int64_t>(i) * kSlotWords + kSlotListOff,
+                  ((m + 1u) / 2u) * 16u, gbar);
+    }
+  };
+  int i0 = 0;
+  int i1 = ns > 0 ? round_end(0) : 0;
+  if (warp == 0 && ns > 0) issue_round(0, i1);
+  // Count windows into the histogram while the copies are in flight.
   for (int j = threadIdx.x; j < ns * kSlotHistBins; j += NT) {
     const int i = j / kSlotHistBins, k = j - i * kSlotHistBins;
     if (k < static_cast<int>(hnb[i])) {
@@ -481,75 +555,73 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
       if (c) atomicAdd(&mh[hlo[i] + k], c);
     }
   }
-  auto round_end = [&](int i0) {
-    int i1 = i0 + 1;
-    while (i1 < ns && hpre[i1 + 1] - hpre[i0] <= static_cast<uint32_t>(kCap)) ++i1;
-    return i1;
-  };
-  auto copy_round = [&](int i0, int i1) {
-    const uint32_t base = hpre[i0];
-    const int np = (i1 - i0) * kPairs;
-    for (int g0 = 0; g0 < np; g0 += kUnroll * NT) {
-      uint4 v[kUnroll];
-      int d[kUnroll];
-#pragma unroll
-      for (int r = 0; r < kUnroll; ++r) {
-        const int g = g0 + r * NT + static_cast<int>(threadIdx.x);
-        d[r] = -1;
-        v[r] = make_uint4(0u, 0u, 0u, 0u);
-        if (g < np) {
-          const int li = g / kPairs;
-          const int j = g - li * kPairs;
-          const int i = i0 + li;
-          const int m = static_cast<int>(hm[i]);
-          if (2 * j < m) {
-            v[r] = *reinterpret_cast<const uint4*>(slots + static_cast<int64_t>(i) * kSlotWords +
-                                                   kSlotListOff + 2 * j);
-            if (2 * j + 1 == m) v[r].z = v[r].w = 0u;  // odd list: zero its padding word
-            d[r] = static_cast<int>(hpre[i] - base) + 2 * j;
-          }
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < kUnroll; ++r)
-        if (d[r] >= 0) *reinterpret_cast<uint4*>(buf + d[r]) = v[r];
-    }
-  };
-  int i0 = 0;
-  int i1 = ns > 0 ? round_end(0) : 0;
-  if (ns > 0) copy_round(0, i1);
   __syncthreads();
   if (warp == 0) {
     uint32_t c;
-    const uint32_t g = warp_find_cut<kTopK>(Hist32{mh}, 0u, scratch[1], &c, lane);
-    if (lane == 0) {
-      scratch[0] = g;
-      scratch[2] = 0u;
-    }
+    // Only counted bins can reach 512; when none does, every published word stays (G = 0).
+    const uint32_t g = warp_find_cut<kTopK>(Hist32{mh}, scratch[3], scratch[1], &c, lane);
+    if (lane == 0) scratch[0] = c >= static_cast<uint32_t>(kTopK) ? g : 0u;
   }
   __syncthreads();
   const uint32_t G = scratch[0], H = scratch[1];
   const uint32_t lt_mask = (1u << lane) - 1u;
+  uint32_t phase = 0u;
   while (i0 < ns) {
-    const int nw = static_cast<int>(hpre[i1] - hpre[i0]);
-    for (int x0 = 0; x0 < nw; x0 += NT) {
-      const int x = x0 + static_cast<int>(threadIdx.x);
-      const uint64_t u = x < nw ? buf[x] : 0ull;
-      const uint32_t bn = hbin(u);
-      const bool keep = u != 0ull && bn >= G && bn <= H;  // every published bin is <= H
-      const uint32_t km = __ballot_sync(0xffffffffu, keep);
-      uint32_t at = 0u;
-      if (lane == 0 && km) at = atomicAdd(&scratch[2], __popc(km));
-      at = __shfl_sync(0xffffffffu, at, 0) + __popc(km & lt_mask);
-      if (keep && at < static_cast<uint32_t>(kSurvCap)) ra.sv[at] = u;
+    if (!mbar_wait(gbar, phase, abort_flag, p.err)) {
+      mbar_drain(gbar, phase);  // never exit with copies in flight
+      return;
+    }
+    const uint32_t base = hpre[i0];
+    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += NT)
+      if (hm[i] & 1u) buf[hpre[i] - base + hm[i]] = 0ull;  // an odd list's padding word
+    __syncthreads();
+    // Keep the words with bin in [G, H], compacted in two passes (count per warp stripe, then
+    // write at the stripe's offset), so no pass waits on a returning atomic.
+    const int nwords = static_cast<int>(hpre[i1] - base);
+    const int per_warp = (nwords + kWarps - 1) / kWarps;
+    const int lo = warp * per_warp, hi = lo + per_warp < nwords ? lo + per_warp : nwords;
+    uint32_t cnt = 0u;
+    for (int x = lo; x < hi; x += 128) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = x + r * 32 + lane;
+        const uint64_t u = i < hi ? buf[i] : 0ull;
+        const uint32_t bn = hbin(u);
+        cnt += __popc(__ballot_sync(0xffffffffu, u != 0ull && bn >= G && bn <= H));
+      }
+    }
+    if (lane == 0) wcnt[warp] = cnt;
+    __syncthreads();
+    uint32_t pos = scratch[2];
+    for (int w = 0; w < warp; ++w) pos += wcnt[w];
+    for (int x = lo; x < hi; x += 128) {
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = x + r * 32 + lane;
+        const uint64_t u = i < hi ? buf[i] : 0ull;
+        const uint32_t bn = hbin(u);
+        const bool keep = u != 0ull && bn >= G && bn <= H;  // every published bin is <= H
+        const uint32_t km = __ballot_sync(0xffffffffu, keep);
+        const uint32_t at = pos + __popc(km & lt_mask);
+        if (keep && at < static_cast<uint32_t>(kSurvCap)) ra.sv[at] = u;
+        pos += __popc(km);
+      }
     }
     __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t tot = scratch[2];
+      for (int w = 0; w < kWarps; ++w) tot += wcnt[w];
+      scratch[2] = tot;
+    }
+    phase ^= 1u;
     i0 = i1;
     if (i0 < ns) {
       i1 = round_end(i0);
-      copy_round(i0, i1);
+      fence_proxy_async_smem();
       __syncthreads();
+      if (warp == 0) issue_round(i0, i1);
     }
+    __syncthreads();
   }
   const int n_sv = static_cast<int>(scratch[2]);
   __syncthreads();
@@ -647,10 +719,11 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint8_t* sK = smem + C::kOffK;
   float* sW = reinterpret_cast<float*>(smem + C::kOffW);
   float* sScore = reinterpret_cast<float*>(smem + C::kOffRing);
-  // buffered mode only: scores, candidate bitmap, per-bin counts
+  // buffered mode only: scores, candidate offsets, per-bin counts
   float* sBuf = reinterpret_cast<float*>(smem + C::kOffBuf);
-  uint32_t* s_bits = reinterpret_cast<uint32_t*>(smem + C::kOffBits);
+  uint16_t* s_cand = reinterpret_cast<uint16_t*>(smem + C::kOffCand);
   uint32_t* s_bins = reinterpret_cast<uint32_t*>(smem + C::kOffBins);
+  uint32_t* s_grp = s_bins + kHBins / 2;  // 32-bin group counts
   uint64_t* sPool = reinterpret_cast<uint64_t*>(smem + C::kOffPool);
   uint32_t* sHist = reinterpret_cast<uint32_t*>(smem + C::kOffHist);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBar);
@@ -661,6 +734,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint64_t* sfull = tempty + C::kAccBufs;        // [C::kScoreBufs] epilogue -> selectors
   uint64_t* sempty = sfull + C::kScoreBufs;         // [C::kScoreBufs] selectors -> epilogue
   uint64_t* qfull = sempty + C::kScoreBufs;         // Q block landed
+  uint64_t* gbar = qfull + 1;                       // slot merge: bulk copies landed
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 4);
   volatile uint32_t* s_last = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
@@ -669,10 +743,11 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   // Running threshold published by each selector warp (only rises): a query's warps filter
   // against the largest of them, which is still at most the CTA's exact 512th best.
   volatile uint64_t* s_theta = reinterpret_cast<volatile uint64_t*>(smem + C::kOffMisc + 64);
-  // Buffered mode: running cut bin (only rises), candidates so far, highest candidate bin.
+  // Buffered mode: running cut bin (only rises), the highest candidate bin, and the number of
+  // candidates each epilogue warp listed.
   uint32_t* s_cut = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 96);
-  uint32_t* s_cand = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 100);
-  uint32_t* s_maxbin = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 104);
+  uint32_t* s_maxbin = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 100);
+  uint32_t* s_ncand = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 104);  // [kEpiWarps]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -719,10 +794,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       mbar_init(&sempty[i], C::kSelectors > 0 ? C::kSelectors : 1);  // unused without selectors
     }
     mbar_init(qfull, 1);
+    mbar_init(gbar, 1);
     *s_abort = 0u;
     for (int i = 0; i < C::kSelectors; ++i) s_theta[i] = 0ull;
     *s_cut = 0u;
-    *s_cand = 0u;
     *s_maxbin = 0u;
     fence_mbar_init();
   }
@@ -825,6 +900,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       return (tile < n_tiles && k < p.S) ? __ldg(kscale_b + k) : 0.f;
     };
     float ks_next0 = 1.f, ks_next1 = 1.f;
+    uint32_t own_cand = 0u;                                  // buffered mode: keys listed
+    uint16_t* own_list = s_cand + warp * C::kCandSeg;        // buffered mode: their offsets
     if (DT == kDtFp8) {
       ks_next0 = load_scale(it0);
       ks_next1 = load_scale(it0 + step);
@@ -887,26 +964,29 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
               p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
             }
           } else if (buffered) {
-            sBuf[it * kTileKeys + quad * 32 + lane] = score;
             // Running cut: a key is a candidate when its bin reaches the cut bin, which some
-            // 512 candidates already reach (so it never exceeds the bin of the CTA's 512th
-            // best). Candidates are marked in the bitmap and counted per bin; every kRecut
-            // candidates the warp that crosses the mark raises the cut from the counts.
+            // 512 candidates already reach (so the cut never passes the bin of the CTA's 512th
+            // best). Candidates are counted per bin and listed; after every kRecut candidates
+            // of its own a warp raises the cut from the counts (which only grow, so any value
+            // read is a lower bound and the cut stays valid).
+            const int k = it * kTileKeys + quad * 32 + lane;
+            sBuf[k] = score;
             const uint64_t u = key < vis_q ? pack_key(score, static_cast<uint32_t>(key)) : 0ull;
             const uint32_t bn = hbin(u);
             const bool keep = u != 0ull && bn >= *reinterpret_cast<volatile uint32_t*>(s_cut);
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
-            if (lane == 0) s_bits[it * (kTileKeys / 32) + quad] = km;
             if (km) {
-              if (keep) hist16_inc(s_bins, bn);
-              const uint32_t mb = __reduce_max_sync(0xffffffffu, keep ? bn : 0u);
-              uint32_t before = 0u;
-              if (lane == 0) {
-                atomicMax(s_maxbin, mb);
-                before = atomicAdd(s_cand, static_cast<uint32_t>(__popc(km)));
+              if (keep) {
+                hist16_inc(s_bins, bn);
+                atomicAdd(&s_grp[bn >> 5], 1u);
+                const uint32_t pos = own_cand + __popc(km & ((1u << lane) - 1u));
+                if (pos < static_cast<uint32_t>(C::kCandSeg)) own_list[pos] = static_cast<uint16_t>(k);
               }
-              before = __shfl_sync(0xffffffffu, before, 0);
-              if ((before + __popc(km)) / kRecut != before / kRecut) {
+              const uint32_t before = own_cand;
+              own_cand += static_cast<uint32_t>(__popc(km));
+              const uint32_t mb = __reduce_max_sync(0xffffffffu, keep ? bn : 0u);
+              if (lane == 0) atomicMax(s_maxbin, mb);
+              if (own_cand / kRecut != before / kRecut) {
                 __syncwarp();
                 uint32_t lo = 0u, hi = 0u, cnt;
                 if (lane == 0) {
@@ -915,8 +995,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                 }
                 lo = __shfl_sync(0xffffffffu, lo, 0);
                 hi = __shfl_sync(0xffffffffu, hi, 0);
-                const uint32_t nb = warp_find_cut<kTopK>(Hist16{s_bins}, lo, hi, &cnt, lane);
-                if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK)) atomicMax(s_cut, nb);
+                const uint32_t nb =
+                    warp_find_cut_grouped<kTopK>(s_bins, s_grp, lo, hi >= lo ? hi : lo, &cnt, lane);
+                if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK) && nb > lo) atomicMax(s_cut, nb);
               }
             }
           } else {
@@ -932,6 +1013,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         if (!DENSE && !buffered) mbar_arrive(&sfull[sb]);
       }
     }
+    if (buffered && lane == 0) s_ncand[warp] = own_cand;
   } else if (!DENSE) {
     // ================= selectors
     const int sidx = warp - C::kSelWarp0;
@@ -1005,7 +1087,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   }
   if (!DENSE && !*s_abort) {
     if (buffered)
-      finish_hist<C>(p, b, t0, split, s_bins, s_bits, sBuf, n_tiles,
+      finish_hist<C>(p, b, t0, split, s_bins, s_cand, s_ncand, sBuf, n_tiles,
                      static_cast<int64_t>(tile_lo) * kTileKeys, vis_q, *s_cut, *s_maxbin,
                      reinterpret_cast<uint64_t*>(sK), s_scratch, warp, lane);
     else if (C::kSelPerQuery > 1 || p.n_splits > 1)
@@ -1025,8 +1107,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       __threadfence();
       if (!*s_abort) {
         if constexpr (C::kHistSel)
-          merge_hist_slots<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), smem + C::kOffHist,
-                              s_scratch, warp, lane);
+          merge_hist_slots<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), smem + C::kOffHist, gbar,
+                              s_abort, s_scratch, warp, lane);
         else
           merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch, warp,
                                lane);
