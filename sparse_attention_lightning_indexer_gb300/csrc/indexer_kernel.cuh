@@ -45,7 +45,9 @@ constexpr int kDtFp8 = 1;
 //   words 2..129  a window of 256 32-bit counts of the published words per bin (histsel.cuh),
 //                 bins lo .. lo + nb - 1; bins below the window may go uncounted (an undercount
 //                 can only lower the merge's cut bin, never drop a winner)
-//   words 130..   the m published words, unordered (m <= kSlotListCap)
+//   words 130..   the m published words (m <= kSlotListCap), grouped by bin: the window's bins
+//                 from the highest down, each bin's words in any order, then every word below
+//                 the window; so the words at or above any bin of the window form a prefix
 // A split publishes every word of its keys whose bin is at or above a bin that at least 512 of
 // its words reach: a superset of its 512 best, hence of every global winner among its keys.
 constexpr int kSlotHdrWords = 2;
@@ -182,13 +184,38 @@ __device__ __forceinline__ void write_output(const KParams& p, int64_t row,
   }
 }
 
-// Publishes cnt (<= 512) words as a one-query split's slot, with a histogram window counted
-// from the words themselves (the 256 bins up to the highest bin present). `tmp`: 256 words.
+// Bucket positions for a bin-grouped slot list (one warp): bucket r < nb holds bin whi - r, the
+// last bucket (r = nb) every word below the window. cur[r] receives the number of words in
+// buckets before r; cnt(bin) gives the exact count of each window bin.
+template <class Cnt>
+__device__ __forceinline__ void slot_bucket_starts(const Cnt cnt, uint32_t whi, int nb,
+                                                   uint32_t* cur, int lane) {
+  uint32_t acc = 0u;
+  for (int r0 = 0; r0 < nb; r0 += 32) {
+    const int r = r0 + lane;
+    const uint32_t c = r < nb ? cnt(whi - static_cast<uint32_t>(r)) : 0u;
+    uint32_t s = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += v;
+    }
+    if (r < nb) cur[r] = acc + s - c;
+    acc += __shfl_sync(0xffffffffu, s, 31);
+  }
+  if (lane == 0) cur[nb] = acc;
+}
+
+// Publishes cnt (<= 512) words as a one-query split's slot, grouped by bin, with a histogram
+// window counted from the words themselves (the 256 bins up to the highest bin present).
+// `tmp`: 2 * 257 words of shared scratch.
 template <int NT>
 __device__ void publish_slot(uint64_t* slot, const uint64_t* words, int cnt, uint32_t* tmp,
-                             uint32_t* scratch, int lane) {
+                             uint32_t* scratch, int warp, int lane) {
+  uint32_t* counts = tmp;        // [256]
+  uint32_t* cur = tmp + 257;     // [257]
   if (threadIdx.x == 0) scratch[0] = 0u;
-  for (int i = threadIdx.x; i < kSlotHistBins; i += NT) tmp[i] = 0u;
+  for (int i = threadIdx.x; i < kSlotHistBins; i += NT) counts[i] = 0u;
   __syncthreads();
   uint32_t mb = 0u;
   for (int i = threadIdx.x; i < cnt; i += NT) mb = max(mb, hbin(words[i]));
@@ -197,15 +224,22 @@ __device__ void publish_slot(uint64_t* slot, const uint64_t* words, int cnt, uin
   __syncthreads();
   const uint32_t hi = scratch[0];
   const uint32_t lo = hi >= kSlotHistBins - 1 ? hi - (kSlotHistBins - 1) : 0u;
+  const int nb = cnt > 0 ? static_cast<int>(hi - lo) + 1 : 0;
   for (int i = threadIdx.x; i < cnt; i += NT) {
     const uint32_t bn = hbin(words[i]);
-    if (bn >= lo) atomicAdd(&tmp[bn - lo], 1u);
+    if (bn >= lo) atomicAdd(&counts[bn - lo], 1u);
   }
   __syncthreads();
-  const uint32_t nb = cnt > 0 ? hi - lo + 1 : 0u;
+  if (warp == 0) slot_bucket_starts(Hist32{counts}, hi - lo, nb, cur, lane);  // bins as offsets
+  __syncthreads();
+  for (int i = threadIdx.x; i < cnt; i += NT) {
+    const uint64_t u = words[i];
+    const uint32_t bn = hbin(u);
+    const int r = bn >= lo ? static_cast<int>(hi - bn) : nb;
+    slot[kSlotListOff + atomicAdd(&cur[r], 1u)] = u;
+  }
   uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
-  for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = tmp[i];
-  for (int i = threadIdx.x; i < cnt; i += NT) slot[kSlotListOff + i] = words[i];
+  for (int i = threadIdx.x; i < nb; i += NT) sh[i] = counts[i];
   if (threadIdx.x == 0)
     slot[0] = static_cast<uint64_t>(cnt) | (static_cast<uint64_t>(lo) << 32) |
               (static_cast<uint64_t>(nb) << 48);
@@ -236,7 +270,7 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
     if (p.n_splits > 1) {
       if constexpr (C::kHistSel) {
         publish_slot<C::kThreads>(p.partial + (row * p.n_splits + split) * kSlotWords, stage, cnt,
-                                  hist, scratch, lane);
+                                  hist, scratch, warp, lane);
       } else {
         uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
         for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
@@ -256,26 +290,34 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
   }
 }
 
-// Writes the (up to) 512 best of the n distinct words ra.sv[0..n) as output row `row`, best
-// first. Every word's bin lies in [lo, hi], hi - lo < kRankBins. Words are bucketed by their
-// bin refined with e more bits of the code (e as large as kRankBins buckets allow), a counting
-// sort over the buckets (best first, CTA-wide suffix scan) gives each bucket its range of
-// positions, and a word's final position is its bucket's first position plus the number of
-// larger words in the same bucket (buckets hold a few words). Buckets that start at or after
-// position 512 are not ranked.
+// Writes the (up to) 512 best of the distinct words in ra.sv[0..n) whose bins lie in [lo, hi]
+// (others, such as zero padding, are skipped) as output row `row`, best first; hi - lo <
+// kRankBins. Words are bucketed by their bin refined with e more bits of the code (e as large
+// as kRankBins buckets allow); a counting sort over the buckets (best first, CTA-wide suffix
+// scan) gives each bucket its range of positions, and a word's final position is its bucket's
+// first position plus the number of larger words in the same bucket (buckets hold a few words).
+// Buckets that start at or after position 512 are not ranked.
 template <int NT>
 __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, int n, uint32_t lo,
                            uint32_t hi, int warp, int lane) {
   constexpr int kWarps = NT / 32;
+  static_assert(kWarps + 1 <= 256, "per-warp sums fit the radix scratch");
   int e = 0;
   while (e < 20 && ((static_cast<int>(hi - lo) + 1) << (e + 1)) <= kRankBins) ++e;
   const int range = (static_cast<int>(hi - lo) + 1) << e;
   const int shift = 52 - e;
   const uint64_t base = static_cast<uint64_t>(lo) << e;
+  auto in_range = [&](uint64_t u) {
+    const uint32_t bn = hbin(u);
+    return u != 0ull && bn >= lo && bn <= hi;
+  };
   auto bucket = [&](uint64_t u) { return static_cast<int>((u >> shift) - base); };
   for (int i = threadIdx.x; i < range; i += NT) ra.cnt[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += NT) atomicAdd(&ra.cnt[bucket(ra.sv[i])], 1u);
+  for (int i = threadIdx.x; i < n; i += NT) {
+    const uint64_t u = ra.sv[i];
+    if (in_range(u)) atomicAdd(&ra.cnt[bucket(u)], 1u);
+  }
   __syncthreads();
   // off[r] = words in buckets above r. Thread t owns the buckets v = t*per .. t*per+per-1 counted
   // from the top (r = range-1-v); a block-wide exclusive prefix of the per-thread sums follows.
@@ -299,15 +341,17 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
     ra.cur[r] = run;
     run += ra.cnt[r];
   }
+  if (threadIdx.x == NT - 1) ra.rhist[kWarps] = run;  // words in range
   __syncthreads();
+  const int nv = static_cast<int>(ra.rhist[kWarps]);
   for (int i = threadIdx.x; i < n; i += NT) {
     const uint64_t u = ra.sv[i];
-    ra.sorted[atomicAdd(&ra.cur[bucket(u)], 1u)] = u;
+    if (in_range(u)) ra.sorted[atomicAdd(&ra.cur[bucket(u)], 1u)] = u;
   }
   __syncthreads();
   int32_t* oi = p.out_idx + row * kTopK;
   float* os = p.out_score ? p.out_score + row * kTopK : nullptr;
-  for (int i = threadIdx.x; i < n; i += NT) {
+  for (int i = threadIdx.x; i < nv; i += NT) {
     const uint64_t u = ra.sorted[i];
     const int r = bucket(u);
     const int o = static_cast<int>(ra.off[r]);
@@ -321,11 +365,10 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
       }
     }
   }
-  for (int i = n + threadIdx.x; i < kTopK; i += NT) {
+  for (int i = nv + threadIdx.x; i < kTopK; i += NT) {
     oi[i] = -1;
     if (os) os[i] = -__int_as_float(0x7f800000);
   }
-  static_assert(kWarps <= 256, "per-warp sums fit the radix scratch");
   __syncthreads();
 }
 
@@ -378,59 +421,63 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
   const bool fast = listed && (split_plan ? m <= kSlotListCap
                                           : (m <= kSurvCap && maxbin - bstar < kRankBins));
   if (fast) {
-    uint64_t* dst = split_plan ? slot + kSlotListOff : ra.sv;
-    const uint32_t dst_cap = split_plan ? kSlotListCap : kSurvCap;  // never reached: m words match
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    // The lists side by side: position i is entry i % kCandSeg of list i / kCandSeg. Two passes
-    // over a stripe per warp (count, then write at the warp's offset), no shared atomics.
+    // The lists side by side: position i is entry i % kCandSeg of list i / kCandSeg.
     constexpr int kSpan = kSegs * C::kCandSeg;
-    constexpr int kPerWarp = (kSpan + kWarps - 1) / kWarps;
-    const int lo = warp * kPerWarp, hi = lo + kPerWarp < kSpan ? lo + kPerWarp : kSpan;
-    auto word_at = [&](int i, uint32_t& km) -> uint64_t {
-      uint64_t u = 0ull;
-      if (i < hi) {
-        const int s = i / C::kCandSeg;
-        if (static_cast<uint32_t>(i - s * C::kCandSeg) < ncand[s]) {
-          const int k = cand[i];
-          u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
+    auto word_at = [&](int i) -> uint64_t {
+      const int s = i / C::kCandSeg;
+      if (static_cast<uint32_t>(i - s * C::kCandSeg) >= ncand[s]) return 0ull;
+      const int k = cand[i];
+      const uint64_t u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
+      return hbin(u) >= bstar ? u : 0ull;
+    };
+    if (split_plan) {
+      // Grouped by bin (window bins from the top, then the rest) straight into the slot.
+      const uint32_t wlo = maxbin - bstar >= static_cast<uint32_t>(kSlotHistBins)
+                               ? maxbin - (kSlotHistBins - 1) : bstar;
+      const int nb = m > 0 ? static_cast<int>(maxbin - wlo) + 1 : 0;
+      if (warp == 0) slot_bucket_starts(Hist16{bins}, maxbin, nb, ra.cur, lane);
+      __syncthreads();
+      uint64_t* dst = slot + kSlotListOff;
+#pragma unroll 2
+      for (int i = threadIdx.x; i < kSpan; i += NT) {
+        const uint64_t u = word_at(i);
+        if (u) {
+          const uint32_t bn = hbin(u);
+          const int r = bn >= wlo ? static_cast<int>(maxbin - bn) : nb;
+          const uint32_t pos = atomicAdd(&ra.cur[r], 1u);
+          if (pos < static_cast<uint32_t>(kSlotListCap)) dst[pos] = u;  // never reached: m fit
         }
       }
-      km = __ballot_sync(0xffffffffu, u != 0ull && hbin(u) >= bstar);
-      return u;
-    };
-    uint32_t cnt = 0u;
-    for (int x = lo; x < hi; x += 32) {
-      uint32_t km;
-      word_at(x + lane, km);
-      cnt += __popc(km);
-    }
-    uint32_t* wcnt = ra.rhist;  // not part of sv
-    if (lane == 0) wcnt[warp] = cnt;
-    __syncthreads();
-    uint32_t at = 0u;
-    for (int w = 0; w < warp; ++w) at += wcnt[w];
-    if (warp == kWarps - 1 && lane == 0) scratch[2] = at + cnt;
-    for (int x = lo; x < hi; x += 32) {
-      uint32_t km;
-      const uint64_t u = word_at(x + lane, km);
-      const uint32_t pos = at + __popc(km & lt_mask);
-      if ((km >> lane) & 1u && pos < dst_cap) dst[pos] = u;
-      at += __popc(km);
-    }
-    __syncthreads();
-    const int got = min(static_cast<int>(scratch[2]), static_cast<int>(dst_cap));
-    if (split_plan) {
-      const uint32_t wlo =
-          maxbin - bstar >= static_cast<uint32_t>(kSlotHistBins) ? maxbin - (kSlotHistBins - 1) : bstar;
-      const uint32_t nb = got > 0 ? maxbin - wlo + 1 : 0u;
       uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
-      for (int i = threadIdx.x; i < static_cast<int>(nb); i += NT) sh[i] = Hist16{bins}(wlo + i);
+      for (int i = threadIdx.x; i < nb; i += NT) sh[i] = Hist16{bins}(wlo + i);
       if (threadIdx.x == 0)
-        slot[0] = static_cast<uint64_t>(got) | (static_cast<uint64_t>(wlo) << 32) |
+        slot[0] = static_cast<uint64_t>(m) | (static_cast<uint64_t>(wlo) << 32) |
                   (static_cast<uint64_t>(nb) << 48);
       __syncthreads();
     } else {
-      rank_write<NT>(p, row, ra, got, bstar, maxbin, warp, lane);
+      // Two passes over a stripe per warp (count, then write at the warp's offset) into sv.
+      constexpr int kPerWarp = (kSpan + kWarps - 1) / kWarps;
+      const int lo = warp * kPerWarp, hi = lo + kPerWarp < kSpan ? lo + kPerWarp : kSpan;
+      const uint32_t lt_mask = (1u << lane) - 1u;
+      uint32_t cnt = 0u;
+      for (int x = lo; x < hi; x += 32) {
+        const uint64_t u = x + lane < hi ? word_at(x + lane) : 0ull;
+        cnt += __popc(__ballot_sync(0xffffffffu, u != 0ull));
+      }
+      uint32_t* wcnt = ra.rhist;  // not part of sv
+      if (lane == 0) wcnt[warp] = cnt;
+      __syncthreads();
+      uint32_t at = 0u;
+      for (int w = 0; w < warp; ++w) at += wcnt[w];
+      for (int x = lo; x < hi; x += 32) {
+        const uint64_t u = x + lane < hi ? word_at(x + lane) : 0ull;
+        const uint32_t km = __ballot_sync(0xffffffffu, u != 0ull);
+        const uint32_t pos = at + __popc(km & lt_mask);
+        if (u && pos < static_cast<uint32_t>(kSurvCap)) ra.sv[pos] = u;  // m <= kSurvCap words
+        at += __popc(km);
+      }
+      __syncthreads();
+      rank_write<NT>(p, row, ra, m, bstar, maxbin, warp, lane);
     }
   } else {
     constexpr int kStageWords = C::kStages * C::kKBytes / 8;
@@ -439,7 +486,7 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
                                                   n_tiles * kTileKeys, stage, stage + kTopK,
                                                   kStageWords - kTopK, hist, scratch);
     if (split_plan) {
-      publish_slot<NT>(slot, stage, cnt, hist, scratch, lane);
+      publish_slot<NT>(slot, stage, cnt, hist, scratch, warp, lane);
     } else {
       constexpr int R = kTopK / 32;
       if (warp == 0) {
@@ -458,12 +505,14 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
   }
 }
 
-// One-query split plans, part 2 (the CTA that takes the last ticket). The splits' count windows
-// are summed into one histogram, whose scan gives the highest bin G that at least 512 published
-// words reach; the 512th best word overall lies in G or above. The lists are brought into
-// shared memory by bulk copies (in rounds when they do not fit at once; one round trip each),
-// the words with bin >= G are compacted and rank_write orders them. More survivors than the
-// ranking takes fall back to a radix select over all lists and one CTA-wide sort.
+// One-query split plans, part 2 (the CTA that takes the last ticket). One bulk copy per split
+// brings its header and count window into shared memory; the windows are summed into one
+// histogram, whose scan gives the highest bin G that at least 512 published words reach (the
+// 512th best word overall lies in G or above). Each list is grouped by bin, so its words at or
+// above G are a prefix whose length its window gives (a whole list when G lies below its
+// window); a second round of bulk copies brings just those prefixes, and rank_write orders the
+// words with bin >= G. More of them than the ranking takes fall back to a radix select over all
+// lists and one CTA-wide sort.
 template <class C>
 __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* buf,
                                  uint8_t* area, uint64_t* gbar, volatile uint32_t* abort_flag,
@@ -471,18 +520,34 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
   constexpr int NT = C::kThreads;
   constexpr int kWarps = NT / 32;
   constexpr int kCap = C::kStages * C::kKBytes / 8;  // words of the gather area
+  constexpr int kHead = kSlotListOff;                // header + window words of a slot
+  static_assert(64 * kHead <= kCap, "every split's header and window fit at once");
   const RankArea ra(area);
-  uint32_t* mh = reinterpret_cast<uint32_t*>(ra.sv);  // kHBins counts; sv is written later
+  uint32_t* mh = reinterpret_cast<uint32_t*>(ra.sv);  // kHBins counts, until sv is filled
   uint32_t* hm = ra.hdr;      // [64] list sizes
   uint32_t* hlo = hm + 64;    // [64] window starts
   uint32_t* hnb = hlo + 64;   // [64] window widths
-  uint32_t* hpre = hnb + 64;  // [65] list offsets in the gather area (sizes rounded up to even)
-  uint32_t* wcnt = ra.rhist;  // [kWarps] survivors per warp
+  uint32_t* hn = hnb + 64;    // [64] words to take from each list
+  uint32_t* hpre = hn + 64;   // [65] their offsets in sv (rounded up to even)
   const int ns = p.n_splits;
   const int64_t row = static_cast<int64_t>(b) * p.T + t0;
   const uint64_t* slots = p.partial + row * ns * kSlotWords;
+  for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
+  fence_proxy_async_smem();  // earlier generic accesses to the copy targets precede the copies
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(ns * kHead * 8));
+    __syncwarp();
+    fence_proxy_async_global();  // the slots published by other CTAs, seen by the copies
+    for (int i = lane; i < ns; i += 32)
+      bulk_load(buf + i * kHead, slots + static_cast<int64_t>(i) * kSlotWords, kHead * 8, gbar);
+  }
+  if (!mbar_wait(gbar, 0u, abort_flag, p.err)) {
+    mbar_drain(gbar, 0u);  // never exit with copies in flight
+    return;
+  }
   for (int i = threadIdx.x; i < ns; i += NT) {
-    const uint64_t h = slots[static_cast<int64_t>(i) * kSlotWords];
+    const uint64_t h = buf[i * kHead];
     const uint32_t m = static_cast<uint32_t>(h);
     const uint32_t lo = static_cast<uint32_t>(h >> 32) & 0xFFFFu;
     const uint32_t nb = static_cast<uint32_t>(h >> 48);
@@ -490,69 +555,26 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
     hlo[i] = lo;
     hnb[i] = (nb <= static_cast<uint32_t>(kSlotHistBins) && lo + nb <= static_cast<uint32_t>(kHBins)) ? nb : 0u;
   }
-  for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
-  fence_proxy_async_smem();  // earlier generic accesses to the gather area precede the copies
   __syncthreads();
-  if (warp == 0) {
-    uint32_t acc = 0u, top = 0u, bottom = kHBins - 1;
-    for (int i0 = 0; i0 < ns; i0 += 32) {
-      const int i = i0 + lane;
-      const uint32_t sz = i < ns ? (hm[i] + 1u) & ~1u : 0u;
-      if (i < ns && hnb[i]) {
-        top = max(top, hlo[i] + hnb[i] - 1u);
-        bottom = min(bottom, hlo[i]);
-      }
-      uint32_t s = sz;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += v;
-      }
-      if (i < ns) hpre[i] = acc + s - sz;
-      acc += __shfl_sync(0xffffffffu, s, 31);
-    }
-    top = __reduce_max_sync(0xffffffffu, top);
-    bottom = __reduce_min_sync(0xffffffffu, bottom);
-    if (lane == 0) {
-      hpre[ns] = acc;
-      scratch[1] = top;
-      scratch[2] = 0u;
-      scratch[3] = bottom < top ? bottom : top;  // lowest counted bin
-    }
-  }
-  __syncthreads();
-  auto round_end = [&](int i0) {
-    int i1 = i0 + 1;
-    while (i1 < ns && hpre[i1 + 1] - hpre[i0] <= static_cast<uint32_t>(kCap)) ++i1;
-    return i1;
-  };
-  // One warp arms the barrier with the round's bytes, then its lanes issue a copy per list.
-  auto issue_round = [&](int i0, int i1) {
-    const uint32_t base = hpre[i0];
-    uint32_t bytes = 0u;
-    for (int i = i0 + lane; i < i1; i += 32) bytes += ((hm[i] + 1u) / 2u) * 16u;
-    bytes = __reduce_add_sync(0xffffffffu, bytes);
-    if (lane == 0) mbar_arrive_expect_tx(gbar, bytes);
-    __syncwarp();
-    fence_proxy_async_global();  // the lists published by other CTAs, seen by the copies
-    for (int i = i0 + lane; i < i1; i += 32) {
-      const uint32_t m = hm[i];
-      if (m)
-        bulk_load(buf + (hpre[i] - base),
-                  slots + static_cast<int64_t>(i) * kSlotWords + kSlotListOff,
-                  ((m + 1u) / 2u) * 16u, gbar);
-    }
-  };
-  int i0 = 0;
-  int i1 = ns > 0 ? round_end(0) : 0;
-  if (warp == 0 && ns > 0) issue_round(0, i1);
-  // Count windows into the histogram while the copies are in flight.
   for (int j = threadIdx.x; j < ns * kSlotHistBins; j += NT) {
     const int i = j / kSlotHistBins, k = j - i * kSlotHistBins;
     if (k < static_cast<int>(hnb[i])) {
-      const uint32_t c = reinterpret_cast<const uint32_t*>(
-          slots + static_cast<int64_t>(i) * kSlotWords + kSlotHdrWords)[k];
+      const uint32_t c = reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords)[k];
       if (c) atomicAdd(&mh[hlo[i] + k], c);
+    }
+  }
+  if (warp == 0) {
+    uint32_t top = 0u, bottom = kHBins - 1;
+    for (int i = lane; i < ns; i += 32)
+      if (hnb[i]) {
+        top = max(top, hlo[i] + hnb[i] - 1u);
+        bottom = min(bottom, hlo[i]);
+      }
+    top = __reduce_max_sync(0xffffffffu, top);
+    bottom = __reduce_min_sync(0xffffffffu, bottom);
+    if (lane == 0) {
+      scratch[1] = top;
+      scratch[3] = bottom < top ? bottom : top;  // lowest counted bin
     }
   }
   __syncthreads();
@@ -564,69 +586,60 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
   }
   __syncthreads();
   const uint32_t G = scratch[0], H = scratch[1];
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  uint32_t phase = 0u;
-  while (i0 < ns) {
-    if (!mbar_wait(gbar, phase, abort_flag, p.err)) {
-      mbar_drain(gbar, phase);  // never exit with copies in flight
+  // Words of list i at or above G: the window's counts from G up (a prefix of the list), or
+  // the whole list when G lies at or below the window's start.
+  for (int i = warp; i < ns; i += kWarps) {
+    uint32_t n;
+    if (G <= hlo[i]) {
+      n = hm[i];
+    } else {
+      const uint32_t* win = reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords);
+      uint32_t s = 0u;
+      for (int k = static_cast<int>(G - hlo[i]) + lane; k < static_cast<int>(hnb[i]); k += 32) s += win[k];
+      n = __reduce_add_sync(0xffffffffu, s);
+      n = n < hm[i] ? n : hm[i];
+    }
+    if (lane == 0) hn[i] = n;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t acc = 0u;
+    for (int i0 = 0; i0 < ns; i0 += 32) {
+      const int i = i0 + lane;
+      const uint32_t sz = i < ns ? (hn[i] + 1u) & ~1u : 0u;
+      uint32_t s = sz;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, s, o);
+        if (lane >= o) s += v;
+      }
+      if (i < ns) hpre[i] = acc + s - sz;
+      acc += __shfl_sync(0xffffffffu, s, 31);
+    }
+    if (lane == 0) hpre[ns] = acc;
+  }
+  fence_proxy_async_smem();  // sv held the summed counts (generic accesses) before the copies
+  __syncthreads();
+  const int total = static_cast<int>(hpre[ns]);
+  if (total <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins)) {
+    if (warp == 0) {
+      if (lane == 0) mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(total) * 8u);
+      __syncwarp();
+      for (int i = lane; i < ns; i += 32) {
+        const uint32_t sz = (hn[i] + 1u) & ~1u;
+        if (sz)
+          bulk_load(ra.sv + hpre[i], slots + static_cast<int64_t>(i) * kSlotWords + kSlotListOff,
+                    sz * 8u, gbar);
+      }
+    }
+    if (!mbar_wait(gbar, 1u, abort_flag, p.err)) {
+      mbar_drain(gbar, 1u);
       return;
     }
-    const uint32_t base = hpre[i0];
-    for (int i = i0 + static_cast<int>(threadIdx.x); i < i1; i += NT)
-      if (hm[i] & 1u) buf[hpre[i] - base + hm[i]] = 0ull;  // an odd list's padding word
+    for (int i = threadIdx.x; i < ns; i += NT)
+      if (hn[i] & 1u) ra.sv[hpre[i] + hn[i]] = 0ull;  // an odd prefix's padding word
     __syncthreads();
-    // Keep the words with bin in [G, H], compacted in two passes (count per warp stripe, then
-    // write at the stripe's offset), so no pass waits on a returning atomic.
-    const int nwords = static_cast<int>(hpre[i1] - base);
-    const int per_warp = (nwords + kWarps - 1) / kWarps;
-    const int lo = warp * per_warp, hi = lo + per_warp < nwords ? lo + per_warp : nwords;
-    uint32_t cnt = 0u;
-    for (int x = lo; x < hi; x += 128) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = x + r * 32 + lane;
-        const uint64_t u = i < hi ? buf[i] : 0ull;
-        const uint32_t bn = hbin(u);
-        cnt += __popc(__ballot_sync(0xffffffffu, u != 0ull && bn >= G && bn <= H));
-      }
-    }
-    if (lane == 0) wcnt[warp] = cnt;
-    __syncthreads();
-    uint32_t pos = scratch[2];
-    for (int w = 0; w < warp; ++w) pos += wcnt[w];
-    for (int x = lo; x < hi; x += 128) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int i = x + r * 32 + lane;
-        const uint64_t u = i < hi ? buf[i] : 0ull;
-        const uint32_t bn = hbin(u);
-        const bool keep = u != 0ull && bn >= G && bn <= H;  // every published bin is <= H
-        const uint32_t km = __ballot_sync(0xffffffffu, keep);
-        const uint32_t at = pos + __popc(km & lt_mask);
-        if (keep && at < static_cast<uint32_t>(kSurvCap)) ra.sv[at] = u;
-        pos += __popc(km);
-      }
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t tot = scratch[2];
-      for (int w = 0; w < kWarps; ++w) tot += wcnt[w];
-      scratch[2] = tot;
-    }
-    phase ^= 1u;
-    i0 = i1;
-    if (i0 < ns) {
-      i1 = round_end(i0);
-      fence_proxy_async_smem();
-      __syncthreads();
-      if (warp == 0) issue_round(i0, i1);
-    }
-    __syncthreads();
-  }
-  const int n_sv = static_cast<int>(scratch[2]);
-  __syncthreads();
-  if (n_sv <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins)) {
-    rank_write<NT>(p, row, ra, n_sv, G, H, warp, lane);
+    rank_write<NT>(p, row, ra, total, G, H, warp, lane);
     return;
   }
   // Rare: too many published words at the cut bin. Exact radix selection over every list,
