@@ -137,9 +137,21 @@ template <int DT, int NQ, bool DENSE>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const KParams& kp, int64_t grid,
                    cudaStream_t stream) {
   using C = KCfg<DT, NQ, DENSE>;
-  indexer_kernel<DT, NQ, DENSE><<<static_cast<unsigned>(grid), C::kThreads, C::kSmemBytes,
-                                  stream>>>(tq, tk, kp);
-  const cudaError_t e = cudaGetLastError();
+  // Programmatic stream serialization: this launch may begin while the previous kernel in the
+  // stream finishes (its CTAs set up shared memory and TMEM, then wait in griddep_wait before
+  // touching global memory), hiding launch latency behind that kernel's tail.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, indexer_kernel<DT, NQ, DENSE>, tq, tk, kp);
+  if (e == cudaSuccess) e = cudaGetLastError();
   if (e == cudaSuccess) g_launches.fetch_add(1, std::memory_order_relaxed);
   return e;
 }

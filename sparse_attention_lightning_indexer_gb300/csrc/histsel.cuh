@@ -17,6 +17,15 @@ constexpr int kHBins = 4096;
 
 __device__ __forceinline__ uint32_t hbin(uint64_t u) { return static_cast<uint32_t>(u >> 52); }
 
+// The lowest score whose word reaches bin b: the float whose order-preserving code is b << 20.
+// Bins below 8 hold no finite score (their codes are NaN patterns and -inf): -inf for them, so
+// a threshold test keeps a superset, never fewer keys, than the bin test.
+__device__ __forceinline__ float bin_floor_score(uint32_t b) {
+  if (b <= 8u) return -__int_as_float(0x7f800000);
+  const uint32_t code = b << 20;
+  return __uint_as_float((code & 0x80000000u) ? (code & 0x7FFFFFFFu) : ~code);
+}
+
 // 16-bit counters packed two per 32-bit word (a CTA counts at most a few ten thousand words).
 __device__ __forceinline__ void hist16_inc(uint32_t* h, uint32_t bin) {
   atomicAdd(&h[bin >> 1], 1u << ((bin & 1u) << 4));

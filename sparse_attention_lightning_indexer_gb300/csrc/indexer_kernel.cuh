@@ -284,10 +284,9 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
     }
     __syncthreads();
   }
-  if (p.n_splits > 1) {  // lists visible GPU-wide (also to bulk copies) before the ticket
-    fence_proxy_async_global();
-    __threadfence();
-  }
+  // Lists are made visible GPU-wide by the ticket's fence (thread 0, after a CTA barrier);
+  // this orders the generic-proxy writes before the bulk copies that will read them.
+  if (p.n_splits > 1) fence_proxy_async_global();
 }
 
 // Writes the (up to) 512 best of the distinct words in ra.sv[0..n) whose bins lie in [lo, hi]
@@ -499,10 +498,9 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
       __syncthreads();
     }
   }
-  if (split_plan) {  // the slot is visible GPU-wide (also to bulk copies) before the ticket
-    fence_proxy_async_global();
-    __threadfence();
-  }
+  // The slot is made visible GPU-wide by the ticket's fence (thread 0, after a CTA barrier);
+  // this orders the generic-proxy writes before the bulk copies that will read them.
+  if (split_plan) fence_proxy_async_global();
 }
 
 // One-query split plans, part 2 (the CTA that takes the last ticket). One bulk copy per split
@@ -761,6 +759,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint32_t* s_cut = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 96);
   uint32_t* s_maxbin = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 100);
   uint32_t* s_ncand = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 104);  // [kEpiWarps]
+  // The cut as a score threshold (bin_floor_score of the cut bin, or lower while it catches up).
+  float* s_cutf = reinterpret_cast<float*>(smem + C::kOffMisc + 136);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -811,6 +811,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     *s_abort = 0u;
     for (int i = 0; i < C::kSelectors; ++i) s_theta[i] = 0ull;
     *s_cut = 0u;
+    *s_cutf = bin_floor_score(0u);
     *s_maxbin = 0u;
     fence_mbar_init();
   }
@@ -824,6 +825,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     tmem_alloc(s_tmem, C::kTmemCols);
     tmem_relinquish();
   }
+  // Everything above touches only this CTA's resources; global memory waits for the previous
+  // kernel in the stream (a no-op unless launched as its programmatic dependent).
+  griddep_wait();
   for (int i = threadIdx.x; i < NQ * kHeads; i += C::kThreads) {
     const int64_t t = t0 + i / kHeads;
     sW[i] = t < p.T ? p.w[(static_cast<int64_t>(b) * p.T + t) * kHeads + (i % kHeads)] : 0.f;
@@ -982,13 +986,13 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
             // best). Candidates are counted per bin and listed; after every kRecut candidates
             // of its own a warp raises the cut from the counts (which only grow, so any value
             // read is a lower bound and the cut stays valid).
+            // The test runs on the score against the cut's threshold; only kept keys are packed.
             const int k = it * kTileKeys + quad * 32 + lane;
             sBuf[k] = score;
-            const uint64_t u = key < vis_q ? pack_key(score, static_cast<uint32_t>(key)) : 0ull;
-            const uint32_t bn = hbin(u);
-            const bool keep = u != 0ull && bn >= *reinterpret_cast<volatile uint32_t*>(s_cut);
+            const bool keep = key < vis_q && score >= *reinterpret_cast<volatile float*>(s_cutf);
             const uint32_t km = __ballot_sync(0xffffffffu, keep);
             if (km) {
+              const uint32_t bn = keep ? hbin(pack_key(score, static_cast<uint32_t>(key))) : 0u;
               if (keep) {
                 hist16_inc(s_bins, bn);
                 atomicAdd(&s_grp[bn >> 5], 1u);
@@ -1010,7 +1014,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                 hi = __shfl_sync(0xffffffffu, hi, 0);
                 const uint32_t nb =
                     warp_find_cut_grouped<kTopK>(s_bins, s_grp, lo, hi >= lo ? hi : lo, &cnt, lane);
-                if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK) && nb > lo) atomicMax(s_cut, nb);
+                if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK) && nb > lo) {
+                  const uint32_t prev = atomicMax(s_cut, nb);
+                  *reinterpret_cast<volatile float*>(s_cutf) = bin_floor_score(max(prev, nb));
+                }
               }
             }
           } else {
@@ -1094,6 +1101,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   __syncwarp();
   tc_fence_before();
   __syncthreads();
+  griddep_launch_dependents();  // the stream is done: the next kernel may start its setup
   if (warp == C::kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, C::kTmemCols);
@@ -1111,6 +1119,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
     uint32_t* ticket = p.counters + static_cast<int64_t>(b) * p.n_qb + qb;
+    __syncthreads();  // every thread's list writes (and proxy fence) precede the ticket
     if (threadIdx.x == 0) {
       __threadfence();
       *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1u : 0u;
