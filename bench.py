@@ -163,13 +163,20 @@ def aggregate(local_ms, units_per_rank, device=None):
 
 
 DECODE = "decode_8x262144"
-JOBS = sorted(inputs.WORKLOADS) + [DECODE]
+# Small configurations of the same kernels, for profiler captures that must stay short.
+PROFILE_JOBS = ["decode_8x32768", "fp8_prefill_16k"]
+JOBS = sorted(inputs.WORKLOADS) + [DECODE] + PROFILE_JOBS
 
 
 def load_job(name):
     """(problems, batched): one problem, or the 8 independent decode sequences."""
     if name == DECODE:
         return inputs.decode_batch(**{k: v for k, v in inputs.DECODE_BATCH.items()}), True
+    if name == "decode_8x32768":
+        return inputs.decode_batch(B=8, S=32768, pos=32767, seed=4), True
+    if name == "fp8_prefill_16k":
+        return [inputs.make(name, T=16384, S=16384, pos_offset=0, seed=3,
+                            dtype=inputs.FP8_E4M3)], False
     return [inputs.workload(name)], False
 
 
