@@ -142,6 +142,8 @@ struct KCfg {
   static constexpr int kOffSelEnd = kOffPool + (DENSE ? 0 : kSelectors * kPool * 8);
   static constexpr int kNumBars = 2 * kStages + 2 * kAccBufs + 2 * kScoreBufs + 2;
   static constexpr int kMiscBytes = 160;
+  // mbarrier waits of one-query CTAs suspend (most warps wait while the epilogue works).
+  static constexpr uint32_t kWaitHint = NQ == 1 ? 20000u : 0u;
   // Buffered selection (one-query CTAs whose key split fits): the epilogue keeps every fp32
   // score of the split, counts the keys that reach a running cut bin per bin (16-bit counters)
   // and lists their offsets (one list per epilogue warp), while a selector warp raises the cut;
@@ -848,7 +850,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       for (; it < n_tiles; ++it) {
         const int st = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1;
-        if (!mbar_wait(&empty[st], ph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait<C::kWaitHint>(&empty[st], ph ^ 1u, s_abort, p.err)) break;
         mbar_arrive_expect_tx(&full[st], C::kKBytes);
         uint8_t* dst = sK + st * C::kKBytes;
         const int32_t key0 = (tile_lo + it) * kTileKeys;
@@ -860,21 +862,21 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       // stage and for the Q block. After a normal run these have long completed.
       const int issued = it;
       for (int j = issued - C::kStages > 0 ? issued - C::kStages : 0; j < issued; ++j)
-        mbar_wait(&full[j % C::kStages], (j / C::kStages) & 1, s_abort, p.err);
-      mbar_wait(qfull, 0, s_abort, p.err);
+        mbar_wait<C::kWaitHint>(&full[j % C::kStages], (j / C::kStages) & 1, s_abort, p.err);
+      mbar_wait<C::kWaitHint>(qfull, 0, s_abort, p.err);
     }
   } else if (warp == C::kMmaWarp) {
     // ================= MMA issuer (one thread)
     if (lane == 0 && n_tiles > 0) {
       int it = 0;
-      bool ok = mbar_wait(qfull, 0, s_abort, p.err);
+      bool ok = mbar_wait<C::kWaitHint>(qfull, 0, s_abort, p.err);
       for (; ok && it < n_tiles; ++it) {
         const int st = it % C::kStages;
         const uint32_t sph = (it / C::kStages) & 1;
         const int acc = it % C::kAccBufs;
         const uint32_t aph = (it / C::kAccBufs) & 1;
-        if (!mbar_wait(&full[st], sph, s_abort, p.err)) break;
-        if (!mbar_wait(&tempty[acc], aph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait<C::kWaitHint>(&full[st], sph, s_abort, p.err)) break;
+        if (!mbar_wait<C::kWaitHint>(&tempty[acc], aph ^ 1u, s_abort, p.err)) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(acc * C::kN);
         const uint32_t a_base = smem_u32(sK + st * C::kKBytes);
@@ -897,7 +899,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       // the last tile issued (the epilogue waits on the same phase).
       if (it > 0) {
         const int last = it - 1;
-        mbar_wait(&tfull[last % C::kAccBufs], (last / C::kAccBufs) & 1, s_abort, p.err);
+        mbar_wait<C::kWaitHint>(&tfull[last % C::kAccBufs], (last / C::kAccBufs) & 1, s_abort, p.err);
       }
     }
     __syncwarp();
@@ -935,10 +937,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         ks_next0 = ks_next1;
         ks_next1 = load_scale(it + 2 * step);
       }
-      if (!mbar_wait_warp(&tfull[acc], aph, s_abort, p.err)) break;
+      if (!mbar_wait_warp<C::kWaitHint>(&tfull[acc], aph, s_abort, p.err)) break;
       tc_fence_after();
       if (!DENSE && !buffered) {
-        if (!mbar_wait_warp(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait_warp<C::kWaitHint>(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
       }
       // The warp's TMEM reads are 2 * kQPerGroup chunks of 32 head columns. Chunk c+1 is
       // requested before chunk c is reduced, so each load's latency hides behind arithmetic
@@ -1051,7 +1053,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     for (int it = 0; it < (buffered ? 0 : n_tiles); ++it) {
       const int sb = it % C::kScoreBufs;
       const uint32_t sph = (it / C::kScoreBufs) & 1;
-      if (!mbar_wait_warp(&sfull[sb], sph, s_abort, p.err)) break;
+      if (!mbar_wait_warp<C::kWaitHint>(&sfull[sb], sph, s_abort, p.err)) break;
       uint64_t th = theta;
 #pragma unroll
       for (int o = 0; o < C::kSelPerQuery; ++o) th = umax64(th, s_theta[q * C::kSelPerQuery + o]);

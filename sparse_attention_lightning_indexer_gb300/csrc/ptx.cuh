@@ -44,15 +44,30 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                "r"(bytes)
                : "memory");
 }
+// kHintNs > 0: the waiting thread may be suspended until the phase completes, for at most
+// that many ns, so a waiting warp takes almost no issue slots from the warps doing the work.
+// That helps where a few warps work while many wait (one-query decode CTAs); where the waits
+// are on the critical path (prefill), the plain test wakes sooner.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
+  if constexpr (kHintNs > 0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "n"(kHintNs)
+        : "memory");
+  } else {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+  }
   return ok != 0;
 }
 
@@ -63,12 +78,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 // Waits for the phase with the given parity to complete. Gives up (returns false) when the
 // CTA-wide abort flag is raised or after kWaitLimitNs, in which case it raises the flag and
 // records the timeout in the global error word.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile uint32_t* abort_flag, uint32_t* err) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait<kHintNs>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait<kHintNs>(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -82,9 +98,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 
 // Warp-collective variant: every lane waits (each gets acquire semantics), and the result is
 // made warp-uniform so callers can branch without divergence.
+template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
                                                volatile uint32_t* abort_flag, uint32_t* err) {
-  const bool ok = mbar_wait(bar, parity, abort_flag, err);
+  const bool ok = mbar_wait<kHintNs>(bar, parity, abort_flag, err);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
