@@ -101,14 +101,15 @@ struct KCfg {
   static constexpr int kN = kHeads * NQ;                             // MMA N
   static constexpr int kQBytes = kN * kRowBytes;
   static constexpr int kKBytes = kTileKeys * kRowBytes;
-  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 3 : 4) : (NQ == 4 ? 6 : 8);
+  static constexpr int kStages = DT == kDtBf16 ? (NQ == 4 ? 2 : 4) : (NQ == 4 ? 6 : 8);
   static constexpr int kKSteps = DT == kDtBf16 ? kDim / 16 : kDim / 32;
   static constexpr int kStepBytes = 32;                              // K bytes per MMA step
   // Depth of the epilogue -> selector score ring: it lets selectors fall behind by that many
-  // tiles while they radix-select, without stalling the MMA pipeline. FP8 tiles arrive twice as
-  // fast (and leave more shared memory), so their ring is deeper; selections cluster at the
-  // start of each query block, while the threshold is still low.
-  static constexpr int kScoreBufs = NQ == 1 ? 16 : (DT == kDtFp8 ? 30 : 12);
+  // tiles while they radix-select, without stalling the MMA pipeline. Selections cluster at the
+  // start of each query block, while the threshold is still low, so a deep ring pays more than
+  // a deep K pipeline: four-query bf16 CTAs keep two K stages (keys come from L2) and 28 ring
+  // tiles.
+  static constexpr int kScoreBufs = NQ == 1 ? 16 : (DT == kDtFp8 ? 30 : 28);
   // TMEM accumulators: all 512 columns, so a narrow (one-query) MMA can run up to 8 tiles
   // ahead of the epilogue instead of waiting on a round trip per tile.
   static constexpr int kAccBufs = 512 / kN;
