@@ -268,3 +268,15 @@ def test_single_query_batched_splits_deterministic(fp8_ix):
         assert torch.equal(idx, idx2) and torch.equal(sc, sc2)
     for b, prob in enumerate(probs):
         parity.check_rows(prob, [0], idx[b].cpu().numpy(), sc[b].cpu().numpy())
+
+
+def test_single_query_clipped_windows(fp8_ix):
+    # 2^50-fold key scales put a split's top bin ~400 bins above its cut: its count window is
+    # clipped to the top 256 bins, its other candidates sit below the window, and the merge's
+    # global cut falls below it, so the merge takes that split's whole list.
+    prob = inputs.make("clip1", T=1, S=30000, pos_offset=29999, seed=53, dtype=inputs.FP8_E4M3)
+    g = torch.Generator().manual_seed(53)
+    pick = torch.randperm(30000, generator=g)[:40]
+    prob.kscale[pick] *= 2.0 ** 50
+    stats, gi, _ = run_full(prob, fp8_ix)
+    assert set(pick.tolist()) <= set(gi[0].tolist())
