@@ -26,6 +26,9 @@
  *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls are asynchronous: they
  *    enqueue kernels on `stream` and return; outputs are valid once the stream has reached that
  *    point. No entry point synchronises the host except ds4idx_sync_status and ds4idx_destroy.
+ *    Kernels are launched as programmatic dependents of the previous kernel on `stream`: their
+ *    blocks may start (shared memory and tensor-memory setup) while that kernel finishes, but
+ *    touch no global memory before it has completed, so stream order holds as usual.
  *  - A handle is not thread-safe: use one handle per stream / host thread. The handle owns a
  *    small device workspace (error word, per-split candidate lists) allocated at create; the
  *    compute entry points allocate nothing.
