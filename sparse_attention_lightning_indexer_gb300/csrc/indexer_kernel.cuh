@@ -6,17 +6,23 @@
 //     I[t,s] = kscale[s] * sum_j w[t,j] * max(0, q[t,j,:] . k[s,:]),  s <= pos_offset + t,
 // keeping per query the 512 largest (score, lower-index-first) pairs.
 //
-// One CTA owns NQ consecutive queries of one sequence (and, when the key range is split, one
-// slice of their keys). Its warps:
-//   epilogue     4 or 8 warps; warp e reads TMEM lanes 32(e%4)..32(e%4)+31, i.e. one key per
-//                thread, for its group of queries, and reduces the 64 head columns of each
-//                query thread-locally (ReLU, * w, sum) with packed fp32x2 FMAs, so the T x S
-//                score matrix never leaves the SM; two warps per lane quadrant hide TMEM latency;
+// One CTA owns NQ (4, or 1 for decode) consecutive queries of one sequence (and, when the key
+// range is split, one slice of their keys). Its warps:
+//   epilogue     8 warps; warp e reads TMEM lanes 32(e%4)..32(e%4)+31, i.e. one key per
+//                thread, for its queries, and reduces the 64 head columns of each query
+//                thread-locally (ReLU, * w, sum) with packed fp32x2 FMAs, so the T x S score
+//                matrix never leaves the SM; two warps per lane quadrant hide TMEM latency
+//                (they split the queries, or take alternate tiles when NQ = 1);
 //   TMA          Q block once, then 128-key K tiles into a ring of stages;
 //   MMA          TMEM owner and MMA issuer: per key tile, D[128 keys, NQ*64 (query, head)]
-//                = K_tile . Q_block^T on tcgen05 into one of two TMEM accumulators;
-//   selectors    one warp per query: filters the tile's scores against the running threshold
-//                into an unsorted pool and radix-selects it back to exactly 512 when it fills.
+//                = K_tile . Q_block^T on tcgen05 into one of the TMEM accumulators (all 512
+//                columns: 2 for NQ = 4, 8 for NQ = 1);
+//   selectors    one warp per query (four for NQ = 1): filter the tile's scores against the
+//                running threshold into an unsorted pool and radix-select it back to exactly
+//                512 when it fills.
+// One-query CTAs whose key split fits shared memory (decode) leave the selectors idle: the
+// epilogue keeps every score and a running cut bin with per-bin counts (histsel.cuh), and the
+// exact selection happens once, at the end (finish_hist, merge_hist_slots).
 // Keys are the MMA M dimension (128 = all TMEM lanes) and (query, head) pairs the N dimension,
 // which is what makes the head reduction free of shuffles. The design on the page (a
 // threadgroup-tiled scorer, then a register-blocked K-resident scorer, then a streaming

@@ -12,8 +12,9 @@
 // the running threshold theta (the exact k-th best word seen so far, 0 before k words were
 // seen). When the pool nears capacity, an exact radix select finds the k-th largest word,
 // compacts the pool to exactly the k largest and raises theta to it. Only the final k words are
-// ever sorted, once, in registers. The page replaced a bitonic sort plus a merge cascade with a
-// streaming Top-512; here no sorting network ever runs on the stream itself.
+// ever sorted, once. The page replaced a bitonic sort plus a merge cascade with a streaming
+// Top-512; here no sorting network ever runs on the stream itself. The CTA-wide selects and the
+// CTA-wide sort below finish split lists and one-query CTAs.
 #pragma once
 #include <cstdint>
 
@@ -431,40 +432,6 @@ template <int K, int NT>
 __device__ __forceinline__ int cta_select(const uint64_t* pool, int n, uint64_t* out,
                                           uint32_t* hist, uint32_t* scratch) {
   return cta_select_get<K, NT>(ArrayWords{pool}, n, out, hist, scratch);
-}
-
-__device__ __forceinline__ void cmp_swap_desc(uint64_t* x, int i, int l) {
-  const uint64_t a = x[i], b = x[l];
-  if (a < b) {
-    x[i] = b;
-    x[l] = a;
-  }
-}
-
-// Sorts a bitonic sequence x[0..N) descending (one warp, shared memory).
-template <int N>
-__device__ __forceinline__ void bitonic_merge_desc(uint64_t* x, int lane) {
-#pragma unroll 1
-  for (int j = N / 2; j > 0; j >>= 1) {
-#pragma unroll
-    for (int p = lane; p < N / 2; p += 32) {
-      const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1));
-      cmp_swap_desc(x, i, i + j);
-    }
-    __syncwarp();
-  }
-}
-
-// a[0..K) and b[0..K) sorted descending; a becomes the K largest of a U b, sorted. One warp.
-template <int K>
-__device__ __forceinline__ void merge_lists(uint64_t* a, const uint64_t* b, int lane) {
-#pragma unroll
-  for (int i = lane; i < K; i += 32) {
-    const uint64_t x = a[i], y = b[K - 1 - i];
-    a[i] = umax64(x, y);
-  }
-  __syncwarp();
-  bitonic_merge_desc<K>(a, lane);
 }
 
 }  // namespace ds4
