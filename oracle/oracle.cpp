@@ -191,8 +191,85 @@ int oracle_topk(int dtype, const void* q, const float* w, const void* k, const f
   return bad ? -1 : 0;
 }
 
+// ---------------------------------------------------------------- FP8 index-cache writer
+// "DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다", section 두 가지 핵심 정확성 수정 사항
+// (FP8 형식 불일치): the indexer key cache is written as FP8 E4M3 and the largest finite value
+// (the "FP8_MAX" of the format) fixes the scale. Here the format is OCP E4M3FN, largest finite
+// 448, with one fp32 scale per token row:
+//     scale = fp32(absmax(row) / 448);  code[i] = E4M3(clamp(fp32(x[i] / scale), -448, 448))
+// rounded to nearest, ties to the even code; a row whose scale is 0 gets codes 0. Query rows
+// get the same rule over all their heads, and their scale is folded into the head weights,
+// w'[t,j] = fp32(w[t,j] * qscale[t]) (exact in the score because ReLU is positively
+// homogeneous). Each fp32 result is the correctly rounded value: the operands are floats, the
+// operation is done in double (53 >= 2 * 24 + 2 bits) and rounded once to float.
+
+// Nearest E4M3FN code to y, by brute force over the 127 positive finite codes (0x00..0x7E);
+// on a tie the code with a zero lowest bit (even mantissa) wins. |y| >= 448 saturates to 448.
+// The sign is kept, so a negative value that rounds to zero gives the negative zero 0x80.
+struct E4M3Table {
+  double v[0x7F];  // value of each positive finite code
+  E4M3Table() {
+    for (int c = 0; c <= 0x7E; ++c) v[c] = decode_e4m3(static_cast<uint8_t>(c));
+  }
+};
+const E4M3Table kE4M3;
+
+uint8_t encode_e4m3(float y) {
+  const uint8_t sign = std::signbit(y) ? 0x80 : 0x00;
+  const double a = std::fabs(static_cast<double>(y));
+  int best = 0;
+  double best_d = a;  // distance to code 0 (value 0)
+  for (int c = 1; c <= 0x7E; ++c) {
+    const double d = std::fabs(kE4M3.v[c] - a);
+    if (d < best_d || (d == best_d && (c & 1) == 0)) {
+      best = c;
+      best_d = d;
+    }
+  }
+  if (a >= 448.0) best = 0x7E;
+  return static_cast<uint8_t>(sign | best);
+}
+
+float round_f32(double v) { return static_cast<float>(v); }
+
+// One row of C values: its scale and codes.
+void quantize_row(const float* x, int64_t C, uint8_t* codes, float* scale) {
+  float absmax = 0.f;
+  for (int64_t i = 0; i < C; ++i) absmax = std::max(absmax, std::fabs(x[i]));
+  const float sc = round_f32(static_cast<double>(absmax) / 448.0);
+  *scale = sc;
+  for (int64_t i = 0; i < C; ++i) {
+    if (sc == 0.f) {
+      codes[i] = 0;
+      continue;
+    }
+    float y = round_f32(static_cast<double>(x[i]) / static_cast<double>(sc));
+    y = std::min(448.f, std::max(-448.f, y));
+    codes[i] = encode_e4m3(y);
+  }
+}
+
 // Exact decoders, exported so tests can pin them against closed forms and library casts.
 double oracle_decode_bf16(uint16_t bits) { return decode_bf16(bits); }
 double oracle_decode_e4m3(uint8_t code) { return decode_e4m3(code); }
+uint8_t oracle_encode_e4m3(float y) { return encode_e4m3(y); }
+
+// Per-row quantisation of x [R, C] (fp32, finite) into codes [R, C] and scales [R].
+// Returns 0, or -1 on a non-finite input.
+int oracle_quantize_rows(const float* x, int64_t R, int64_t C, uint8_t* codes, float* scales) {
+  if (!x || !codes || !scales || R < 0 || C < 1) return -1;
+  for (int64_t i = 0; i < R * C; ++i)
+    if (!std::isfinite(x[i])) return -1;
+#pragma omp parallel for schedule(static)
+  for (int64_t r = 0; r < R; ++r) quantize_row(x + r * C, C, codes + r * C, scales + r);
+  return 0;
+}
+
+// The q-scale fold: w_out[t, j] = fp32(w[t, j] * qscale[t]) for w [T, H].
+void oracle_fold_qscale(const float* w, const float* qscale, int64_t T, int64_t H, float* w_out) {
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t j = 0; j < H; ++j)
+      w_out[t * H + j] = round_f32(static_cast<double>(w[t * H + j]) * static_cast<double>(qscale[t]));
+}
 
 }  // extern "C"

@@ -63,6 +63,12 @@ def _load():
         lib.oracle_decode_bf16.restype = ctypes.c_double
         lib.oracle_decode_e4m3.argtypes = [ctypes.c_uint8]
         lib.oracle_decode_e4m3.restype = ctypes.c_double
+        lib.oracle_encode_e4m3.argtypes = [ctypes.c_float]
+        lib.oracle_encode_e4m3.restype = ctypes.c_uint8
+        lib.oracle_quantize_rows.argtypes = [p, i64, i64, p, p]
+        lib.oracle_quantize_rows.restype = i32
+        lib.oracle_fold_qscale.argtypes = [p, p, i64, i64, p]
+        lib.oracle_fold_qscale.restype = None
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         _lib = lib
@@ -160,3 +166,39 @@ def select(score_rows: np.ndarray, n_visible: np.ndarray, topk: int):
         idx[r, :m] = order[:m]
         sc[r, :m] = row[order[:m]]
     return idx, sc
+
+
+# ---------------------------------------------------------------- FP8 index-cache writer
+
+def encode_e4m3(y: float) -> int:
+    """Nearest OCP E4M3FN code (ties to the even code, saturating at 448, sign kept)."""
+    return int(_load().oracle_encode_e4m3(float(y)))
+
+
+def quantize_rows(x) -> tuple[np.ndarray, np.ndarray]:
+    """Per-row absmax/448 E4M3 quantisation of x [R, C] fp32 -> (codes u8 [R, C], scale f32 [R]).
+
+    scale = fp32(absmax / 448); code = E4M3(clamp(fp32(x / scale), +-448)); scale 0 -> codes 0.
+    ("DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다", FP8 형식 불일치: the FP8 indexer cache.)
+    """
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    if x.ndim != 2:
+        raise ValueError("expected x [R, C]")
+    R, C = x.shape
+    codes = np.empty((R, C), dtype=np.uint8)
+    scales = np.empty((R,), dtype=np.float32)
+    if _load().oracle_quantize_rows(_ptr(x), R, C, _ptr(codes), _ptr(scales)) != 0:
+        raise ValueError("oracle rejected the input (non-finite value or bad shape)")
+    return codes, scales
+
+
+def fold_qscale(w, qscale) -> np.ndarray:
+    """w' [T, H] = fp32(w * qscale[t]) (the query scale folded into the head weights)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    qscale = np.ascontiguousarray(qscale, dtype=np.float32)
+    T, H = w.shape
+    if qscale.shape != (T,):
+        raise ValueError("qscale must be [T]")
+    out = np.empty_like(w)
+    _load().oracle_fold_qscale(_ptr(w), _ptr(qscale), T, H, _ptr(out))
+    return out

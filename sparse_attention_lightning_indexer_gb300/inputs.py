@@ -102,6 +102,16 @@ class Problem:
         return self.q.numpy(), self.k.numpy()
 
 
+def draw_f32(T: int, S: int, seed: int, H: int = H_I, D: int = D_I, parts=("q", "k", "w")):
+    """The fp32 draws of a workload before any rounding: q [T, H, D], k [S, D], w [T, H]
+    (None for a part not in ``parts``). These are the inputs of the FP8 cache writer; ``make``
+    rounds or quantises these same draws."""
+    qf = _randn((T, H, D), _gen(seed, "q"), SIGMA_QK) if "q" in parts else None
+    kf = _randn((S, D), _gen(seed, "k"), SIGMA_QK) if "k" in parts else None
+    w = _randn((T, H), _gen(seed, "w"), SIGMA_W) if "w" in parts else None
+    return qf, kf, w
+
+
 def planted_amplitude(H: int = H_I, D: int = D_I, sigma: float = SIGMA_QK,
                       sigma_w: float = SIGMA_W, n_sigma: float = 3.0) -> float:
     """Topic amplitude that lifts a same-topic pair by n_sigma score std (normal model only)."""
@@ -119,9 +129,7 @@ def make(name: str, T: int, S: int, pos_offset: int, seed: int, dtype: int = BF1
     """Draw one workload. Shapes and distributions follow the module recipe."""
     if T < 0 or S < 1 or pos_offset < 0:
         raise ValueError("bad shape")
-    qf = _randn((T, H, D), _gen(seed, "q"), SIGMA_QK)
-    kf = _randn((S, D), _gen(seed, "k"), SIGMA_QK)
-    w = _randn((T, H), _gen(seed, "w"), SIGMA_W)
+    qf, kf, w = draw_f32(T, S, seed, H, D)
     meta = {"seed": seed}
     if planted:
         a = planted_amplitude(H, D)
