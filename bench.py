@@ -351,7 +351,7 @@ def run_ours(args, rank, world, local_rank):
         ho_idx.copy_(out_idx, non_blocking=True)
         ho_sc.copy_(out_sc, non_blocking=True)
 
-    e2e_steps = max(3, args.steps // 2)
+    e2e_steps = max(3, min(args.steps // 2, 20))
     e2e_step()
     torch.cuda.synchronize()
     if world > 1:
@@ -467,6 +467,17 @@ def main():
         log("warmup raised to 3 (minimum)")
         args.warmup = 3
     rank, world, local_rank = dist_env()
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        # Plain `python bench.py --gpus N`: start N ranks (one process per GPU) under torchrun.
+        cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+               f"--nproc-per-node={args.gpus}", "--master-addr=127.0.0.1",
+               f"--master-port={29500 + os.getpid() % 1000}", os.path.abspath(__file__),
+               *sys.argv[1:]]
+        log("starting", args.gpus, "ranks:", " ".join(cmd))
+        sys.exit(subprocess.call(cmd))
+    if world != args.gpus:
+        log(f"--gpus {args.gpus} disagrees with WORLD_SIZE={world}")
+        sys.exit(2)
     if args.impl == "reference":
         run_reference(args, rank, world)
     else:

@@ -57,7 +57,9 @@ typedef enum {
                                      no-allocation entry point */
 } ds4idx_status;
 
-typedef enum { DS4IDX_BF16 = 0, DS4IDX_FP8_E4M3 = 1 } ds4idx_dtype;
+/* Element types. q and kcache of the indexer are BF16 or FP8_E4M3 codes; F32 is accepted as the
+ * input of the FP8 cache writer only. */
+typedef enum { DS4IDX_BF16 = 0, DS4IDX_FP8_E4M3 = 1, DS4IDX_F32 = 2 } ds4idx_dtype;
 
 typedef struct {
   int32_t n_heads;   /* H_I; must be 64 */
@@ -144,15 +146,19 @@ uint64_t ds4idx_kernels_launched(void);
  * __device__ storage. Every GPU that loads the library holds that array until the process exits.
  *  - dtype is a ds4idx_dtype. All other arguments, layouts and rules are those of
  *    ds4idx_score_topk_batched, with 1 <= B <= 64, 0 <= T, 1 <= S < 2^31 and topk = 512.
- *  - Limit: a call whose key-range split needs more than 2^21 list words (B * T * splits * 512)
- *    returns DS4IDX_ERR_SCRATCH_LIMIT and enqueues nothing. Only short sequences are split
- *    (decode, chunks of a few tokens), and their plans stay well below the limit. Long prefills
- *    are not split and use no scratch.
+ *  - Limit: the array holds 2^21 list words (16 MiB) and the split tickets of 4096 query blocks.
+ *    Short sequences (decode, small chunks) split their key range over several CTAs, and each
+ *    split publishes a list of 512 words per query (1152 per one-query sequence). Here the split
+ *    count steps down from the one ds4idx_score_topk_batched would use until the lists fit
+ *    (B * T * splits * 512 <= 2^21); one split needs no list, so every valid call runs, only
+ *    with fewer CTAs where the handle path would split further. Outputs are the same as the
+ *    handle path's. DS4IDX_ERR_SCRATCH_LIMIT is returned only if a plan still did not fit.
  *  - Set-up: the first call on each device looks up the array's device address and sets kernel
  *    attributes, with that device current. Make that first call before any stream capture.
+ *  - Argument errors return INVALID_ARG before anything is enqueued or the array is touched.
  *  - Sharing: all calls use the same array, and it keeps the previous call's contents. The error
- *    word and the split tickets are cleared on `stream` at the start of every call; the candidate
- *    lists are always fully written before they are read. Calls that can overlap on the GPU (different streams or host
+ *    word and the split tickets are cleared on `stream` at the start of every valid call; the
+ *    candidate lists are always fully written before they are read. Calls that can overlap on the GPU (different streams or host
  *    threads without ordering between them) race on the array and corrupt each other's outputs,
  *    so order them, for example on one stream.
  *  - A kernel that gives up on a bounded device wait records it in the array's error word. This
@@ -162,6 +168,56 @@ int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const void* q, c
                                       const void* kcache, const float* kscale, int64_t T,
                                       int64_t S, const int64_t* pos_offsets, int32_t topk,
                                       int32_t* out_idx, float* out_score, void* stream);
+
+/* ---- FP8 index-cache writer: the step before an FP8 indexer call.
+ * "DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다", section 두 가지 핵심 정확성 수정 사항
+ * (FP8 형식 불일치): the indexer key cache is written as FP8 E4M3, and the format's largest
+ * finite value sets the scale. Here the format is OCP E4M3FN (largest finite 448) with one fp32
+ * scale per token row:
+ *     scale = absmax(row) / 448,  code[i] = E4M3(clamp(x[i] / scale, -448, 448)),
+ * each fp32 operation correctly rounded, the conversion round-to-nearest-even; a row whose
+ * scale is 0 gets codes 0. The results are bit-exact functions of the inputs. Inputs must be
+ * finite. Both calls are asynchronous on `stream` and allocate nothing. */
+
+/* Quantises n new key rows k [n, 128] (in_dtype DS4IDX_F32 or DS4IDX_BF16, 16-byte aligned)
+ * into the index cache: row i goes to cache row slots[i] when `slots` (device int64 [n]) is
+ * given, else to dst_offset + i. kcache [cache_rows, 128] uint8 E4M3 codes (16-byte aligned),
+ * kscale [cache_rows] fp32. Slots outside [0, cache_rows) (e.g. -1 for padding tokens) are
+ * skipped. Errors: INVALID_ARG (dtype, null or misaligned pointer, n < 0, a contiguous range
+ * past cache_rows), LAUNCH. n = 0 is a no-op. */
+int ds4idx_quantize_keys(const void* k, int32_t in_dtype, int64_t n, const int64_t* slots,
+                         int64_t dst_offset, uint8_t* kcache, float* kscale, int64_t cache_rows,
+                         void* stream);
+
+/* Quantises the queries of an FP8 indexer call: q [T, 64, 128] (DS4IDX_F32 or DS4IDX_BF16)
+ * with one scale per token over all 64 x 128 values into q_codes [T, 64, 128] uint8, and folds
+ * the scale into the head weights, w_out[t, j] = w[t, j] * qscale[t] (fp32, correctly rounded;
+ * exact in the score because ReLU is positively homogeneous). w [T, 64] fp32; qscale [T] fp32
+ * receives the scales and may be NULL. w_out may equal w (in place). Errors: INVALID_ARG,
+ * LAUNCH. T = 0 is a no-op. */
+int ds4idx_quantize_queries(const void* q, int32_t in_dtype, int64_t T, const float* w,
+                            uint8_t* q_codes, float* w_out, float* qscale, void* stream);
+
+/* Test support for the bounded device waits (the pages have no counterpart). Every mbarrier
+ * wait in the kernels gives up after a limit (2 s by default), records DS4IDX_ERR_DEVICE_TIMEOUT
+ * for ds4idx_sync_status, waits for its own copies and tensor-core work to finish, frees its
+ * tensor memory and returns, so a lost arrival turns into an error status instead of a hang.
+ * This call sets the limit used by the handle's later calls (1e6 <= wait_limit_ns <= 2e9) and,
+ * with withhold != 0, makes the next calls of a four-query (T > 1) plan without key splits
+ * withhold one arrival of their first CTA's first selector warp, so that CTA's epilogue wait for
+ * the score ring runs out once the ring wraps (more than 30 key tiles in that CTA). Every copy
+ * and MMA already issued completes on its own. Reset with (2000000000, 0).
+ * Errors: INVALID_ARG (null handle, limit out of range). */
+int ds4idx_debug_wait_test(ds4idx_t h, uint64_t wait_limit_ns, int32_t withhold);
+
+/* The work decomposition a call would use, computed on the host alone (no device access), for
+ * tests and capacity planning. num_sms: the device's SM count; B, T, S, pos_offsets[B] as in
+ * ds4idx_score_topk_batched; fixed_scratch != 0 gives the plan of
+ * ds4idx_score_topk_batched_noalloc. out[7] receives: queries per CTA, query blocks per
+ * sequence, key splits, key tiles per split, CTAs in the grid, split-list words, split tickets.
+ * Errors: INVALID_ARG. */
+int ds4idx_plan_query(int32_t num_sms, int32_t B, int64_t T, int64_t S,
+                      const int64_t* pos_offsets, int32_t fixed_scratch, int64_t* out);
 
 #ifdef __cplusplus
 }

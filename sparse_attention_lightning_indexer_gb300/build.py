@@ -1,8 +1,9 @@
 """Builds the ds4idx shared library in-tree (nvcc, sm_103a only).
 
-Output: ``sparse_attention_lightning_indexer_gb300/_lib/libds4idx.so``. The CUDA runtime is
-linked statically; the driver's tensor-map encoder is resolved at run time, so the library
-needs no libcuda at link time and cross-compiles on a machine without a GPU.
+Output: ``sparse_attention_lightning_indexer_gb300/_lib/libds4idx.so``. Every ``csrc/*.cu`` file
+is compiled to an object in parallel, then the objects are linked into one library. The CUDA
+runtime is linked statically; the driver's tensor-map encoder is resolved at run time, so the
+library needs no libcuda at link time and cross-compiles on a machine without a GPU.
 """
 from __future__ import annotations
 
@@ -16,12 +17,22 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libds4idx.so")
-SOURCES = [os.path.join(CSRC, "ds4idx.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "topk.cuh", "indexer_kernel.cuh")] \
-    + [os.path.join(INCLUDE, "ds4idx.h")]
 
-NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-              "-Xcompiler", "-fPIC", "-shared", "--cudart", "static"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-std=c++17", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC"]
+LINK_FLAGS = [*ARCH, "-shared", "--cudart", "static"]
+
+
+def sources() -> list[str]:
+    return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
+
+
+def deps() -> list[str]:
+    """Every file the library is compiled from: the sources, all csrc headers, the C header."""
+    headers = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                     if f.endswith((".cuh", ".h", ".cu")))
+    return sorted(set(sources() + headers + [os.path.join(INCLUDE, f)
+                                             for f in os.listdir(INCLUDE) if f.endswith(".h")]))
 
 
 def nvcc() -> str:
@@ -33,19 +44,36 @@ def up_to_date() -> bool:
     if not os.path.exists(LIB_PATH):
         return False
     t = os.path.getmtime(LIB_PATH)
-    return all(os.path.getmtime(d) <= t for d in DEPS)
+    return all(os.path.getmtime(d) <= t for d in deps())
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB_PATH
     os.makedirs(LIB_DIR, exist_ok=True)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, *SOURCES, "-o", tmp]
-    if verbose:
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB_PATH)
+    tag = f".tmp{os.getpid()}"
+    objs, procs = [], []
+    for src in sources():
+        obj = os.path.join(LIB_DIR, os.path.basename(src)[:-3] + tag + ".o")
+        cmd = [nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC, "-c", src, "-o", obj]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        procs.append((subprocess.Popen(cmd), cmd))
+        objs.append(obj)
+    failed = [cmd for p, cmd in procs if p.wait() != 0]
+    try:
+        if failed:
+            raise subprocess.CalledProcessError(1, failed[0])
+        tmp = LIB_PATH + tag
+        cmd = [nvcc(), *LINK_FLAGS, *objs, "-o", tmp]
+        if verbose:
+            print(" ".join(cmd), file=sys.stderr)
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, LIB_PATH)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
     return LIB_PATH
 
 

@@ -17,6 +17,15 @@
 
 using namespace ds4;
 
+namespace {
+std::atomic<uint64_t> g_launches{0};  // kernels this library has enqueued (process-wide)
+}  // namespace
+
+// Shared with the library's other translation units (their launches are counted too).
+namespace ds4w {
+std::atomic<uint64_t>* launch_counter() { return &g_launches; }
+}  // namespace ds4w
+
 struct ds4idx_handle {
   ds4idx_config cfg;
   int device = 0;
@@ -26,15 +35,20 @@ struct ds4idx_handle {
   size_t partial_words = 0;
   uint32_t* counters = nullptr;   // per-block split tickets, zero between calls
   size_t n_counters = 0;
+  uint64_t wait_ns = 0;           // bounded-wait limit passed to the kernels
+  int32_t withhold = 0;           // test hook (ds4idx_debug_wait_test)
 };
 
 namespace {
 
-constexpr int kVersion = (1 << 16) | 0;
+constexpr int kVersion = (1 << 16) | 1;
+// Fixed scratch of the no-allocation entry point: 2^21 list words (16 MiB) and the split
+// tickets of up to 4096 query blocks.
+constexpr size_t kNoAllocListWords = static_cast<size_t>(1) << 21;
+constexpr size_t kNoAllocTickets = 4096;
 constexpr int kMaxSplits = 64;
 constexpr int kMinTilesPerSplit = 4;
 
-std::atomic<uint64_t> g_launches{0};  // kernels this library has enqueued (process-wide)
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -66,7 +80,14 @@ struct Plan {
   int64_t grid = 0;
 };
 
-Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
+size_t plan_partial_words(const Plan& pl, int64_t B, int64_t T);
+size_t plan_counters(const Plan& pl, int64_t B);
+
+// max_words / max_counters cap the scratch a split plan may use (the fixed array of the
+// no-allocation entry point): the split count steps down until the plan fits; one split needs
+// no scratch at all.
+Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis,
+               size_t max_words = SIZE_MAX, size_t max_counters = SIZE_MAX) {
   Plan pl;
   pl.nq = queries_per_cta(T);
   pl.n_qb = static_cast<int>((T + pl.nq - 1) / pl.nq);
@@ -92,9 +113,16 @@ Plan make_plan(int num_sms, int64_t B, int64_t T, int64_t max_vis) {
       }
     }
   }
-  pl.tiles_per_split = static_cast<int>((tiles + splits - 1) / splits);
-  pl.n_splits = static_cast<int>((tiles + pl.tiles_per_split - 1) / pl.tiles_per_split);
-  if (pl.n_splits < 1) pl.n_splits = 1;
+  for (;; --splits) {
+    pl.tiles_per_split = static_cast<int>(tiles > 0 ? (tiles + splits - 1) / splits : 0);
+    pl.n_splits = pl.tiles_per_split > 0
+                      ? static_cast<int>((tiles + pl.tiles_per_split - 1) / pl.tiles_per_split)
+                      : 1;
+    if (pl.n_splits < 1) pl.n_splits = 1;
+    if (splits <= 1 || (plan_partial_words(pl, B, T) <= max_words &&
+                        plan_counters(pl, B) <= max_counters))
+      break;
+  }
   pl.grid = blocks * pl.n_splits;
   return pl;
 }
@@ -165,16 +193,61 @@ cudaError_t launch_dt(int nq, bool dense, const CUtensorMap& tq, const CUtensorM
   return launch<DT, 4, false>(tq, tk, kp, grid, stream);
 }
 
-// Shared implementation of the three compute entry points.
-int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache,
-        const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
-        int32_t* out_idx, float* out_score, float* dense, void* stream_ptr) {
-  if (!h) return DS4IDX_ERR_INVALID_ARG;
-  const ds4idx_config& c = h->cfg;
+// Scratch and limits one compute call runs with: a handle's workspace, or the fixed array of
+// the no-allocation entry point.
+struct Ctx {
+  int32_t dtype = DS4IDX_BF16;
+  int64_t max_T = 0, max_S = 0, max_batch = 0;
+  int device = 0;
+  int num_sms = 0;
+  uint32_t* err = nullptr;
+  uint64_t* partial = nullptr;
+  size_t partial_words = 0;
+  uint32_t* counters = nullptr;
+  size_t n_counters = 0;
+  bool cap_splits = false;  // fit the split count to the scratch instead of rejecting the call
+  uint64_t wait_ns = kWaitLimitNs;
+  int32_t withhold = 0;
+};
+
+Ctx handle_ctx(const ds4idx_handle* h) {
+  Ctx c;
+  c.dtype = h->cfg.dtype;
+  c.max_T = h->cfg.max_T;
+  c.max_S = h->cfg.max_S;
+  c.max_batch = h->cfg.max_batch;
+  c.device = h->device;
+  c.num_sms = h->num_sms;
+  c.err = h->err;
+  c.partial = h->partial;
+  c.partial_words = h->partial_words;
+  c.counters = h->counters;
+  c.n_counters = h->n_counters;
+  c.wait_ns = h->wait_ns;
+  c.withhold = h->withhold;
+  return c;
+}
+
+// A validated call, ready to enqueue.
+struct Call {
+  Plan pl;
+  CUtensorMap tq, tk;
+  KParams kp;
+  bool dense = false;
+  bool noop = false;  // T = 0
+};
+
+// Validates a compute call and prepares its launch. Enqueues nothing and touches no device
+// memory: every argument error is reported here, before any work is queued.
+int prepare(const Ctx& c, int32_t B, const void* q, const float* w, const void* kcache,
+            const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
+            int32_t* out_idx, float* out_score, float* dense, Call* call) {
   if (B < 1 || B > c.max_batch || B > kMaxBatch) return DS4IDX_ERR_INVALID_ARG;
   if (T < 0 || T > c.max_T || S < 1 || S > c.max_S) return DS4IDX_ERR_INVALID_ARG;
   if (!pos_offsets) return DS4IDX_ERR_INVALID_ARG;
-  if (!dense && topk != c.topk) return DS4IDX_ERR_INVALID_ARG;
+  if (!dense && topk != kTopK) return DS4IDX_ERR_INVALID_ARG;
+  call->dense = dense != nullptr;
+  call->noop = T == 0;
   if (T == 0) return DS4IDX_OK;
   if (!q || !w || !kcache || !aligned16(q) || !aligned16(w) || !aligned16(kcache))
     return DS4IDX_ERR_INVALID_ARG;
@@ -198,9 +271,10 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
   if (!load_encode()) return DS4IDX_ERR_CUDA;
 
   int cur = -1;
-  if (cudaGetDevice(&cur) != cudaSuccess || cur != h->device) return DS4IDX_ERR_INVALID_ARG;
+  if (cudaGetDevice(&cur) != cudaSuccess || cur != c.device) return DS4IDX_ERR_INVALID_ARG;
 
-  Plan pl = make_plan(h->num_sms, B, T, max_vis);
+  Plan pl = c.cap_splits ? make_plan(c.num_sms, B, T, max_vis, c.partial_words, c.n_counters)
+                         : make_plan(c.num_sms, B, T, max_vis);
   if (dense) {
     // Same query blocking as the Top-k path, so the debug scores come from identical MMA tiles.
     pl.nq = queries_per_cta(T);
@@ -209,23 +283,25 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
     pl.tiles_per_split = static_cast<int>((S + kTileKeys - 1) / kTileKeys);
     pl.grid = pl.n_qb;
   }
-  if (plan_partial_words(pl, B, T) > h->partial_words || plan_counters(pl, B) > h->n_counters)
+  if (plan_partial_words(pl, B, T) > c.partial_words || plan_counters(pl, B) > c.n_counters)
+    return c.cap_splits ? DS4IDX_ERR_SCRATCH_LIMIT : DS4IDX_ERR_INVALID_ARG;
+
+  if (!encode_rows(&call->tq, q, c.dtype, T * kHeads, B, kHeads * pl.nq))
     return DS4IDX_ERR_INVALID_ARG;
+  if (!encode_rows(&call->tk, kcache, c.dtype, S, B, kTileKeys)) return DS4IDX_ERR_INVALID_ARG;
 
-  CUtensorMap tq, tk;
-  if (!encode_rows(&tq, q, c.dtype, T * kHeads, B, kHeads * pl.nq)) return DS4IDX_ERR_INVALID_ARG;
-  if (!encode_rows(&tk, kcache, c.dtype, S, B, kTileKeys)) return DS4IDX_ERR_INVALID_ARG;
-
-  KParams kp;
+  KParams& kp = call->kp;
   std::memset(&kp, 0, sizeof kp);
   kp.w = w;
   kp.kscale = kscale;
   kp.out_idx = out_idx;
   kp.out_score = out_score;
-  kp.partial = h->partial;
-  kp.counters = h->counters;
+  kp.partial = c.partial;
+  kp.counters = c.counters;
   kp.dense = dense;
-  kp.err = h->err;
+  kp.err = c.err;
+  kp.wait_ns = c.wait_ns;
+  kp.withhold = c.withhold;
   kp.T = T;
   kp.S = S;
   kp.B = B;
@@ -233,13 +309,32 @@ int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache
   kp.n_splits = pl.n_splits;
   kp.tiles_per_split = pl.tiles_per_split;
   for (int b = 0; b < B; ++b) kp.pos[b] = pos_offsets[b];
-
-  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  cudaError_t e = c.dtype == DS4IDX_BF16
-                      ? launch_dt<kDtBf16>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream)
-                      : launch_dt<kDtFp8>(pl.nq, dense != nullptr, tq, tk, kp, pl.grid, stream);
-  if (e != cudaSuccess) return DS4IDX_ERR_LAUNCH;
+  call->pl = pl;
   return DS4IDX_OK;
+}
+
+int enqueue(const Ctx& c, const Call& call, void* stream_ptr) {
+  if (call.noop) return DS4IDX_OK;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const Plan& pl = call.pl;
+  cudaError_t e =
+      c.dtype == DS4IDX_BF16
+          ? launch_dt<kDtBf16>(pl.nq, call.dense, call.tq, call.tk, call.kp, pl.grid, stream)
+          : launch_dt<kDtFp8>(pl.nq, call.dense, call.tq, call.tk, call.kp, pl.grid, stream);
+  return e == cudaSuccess ? DS4IDX_OK : DS4IDX_ERR_LAUNCH;
+}
+
+// Shared implementation of the handle-based compute entry points.
+int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache,
+        const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
+        int32_t* out_idx, float* out_score, float* dense, void* stream_ptr) {
+  if (!h) return DS4IDX_ERR_INVALID_ARG;
+  const Ctx c = handle_ctx(h);
+  Call call;
+  const int st = prepare(c, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
+                         dense, &call);
+  if (st != DS4IDX_OK) return st;
+  return enqueue(c, call, stream_ptr);
 }
 
 }  // namespace
@@ -297,6 +392,7 @@ int ds4idx_create(ds4idx_t* out, const ds4idx_config* cfg) {
   h->cfg = *cfg;
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
+  h->wait_ns = kWaitLimitNs;
 
   // Workspace for the largest per-split candidate set any admissible call can need.
   size_t words = 0, counters = 0;
@@ -370,6 +466,35 @@ int ds4idx_sync_status(ds4idx_t h, void* stream) {
   return DS4IDX_OK;
 }
 
+int ds4idx_debug_wait_test(ds4idx_t h, uint64_t wait_limit_ns, int32_t withhold) {
+  if (!h || wait_limit_ns < 1000000ull || wait_limit_ns > kWaitLimitNs) return DS4IDX_ERR_INVALID_ARG;
+  h->wait_ns = wait_limit_ns;
+  h->withhold = withhold ? 1 : 0;
+  return DS4IDX_OK;
+}
+
+int ds4idx_plan_query(int32_t num_sms, int32_t B, int64_t T, int64_t S,
+                      const int64_t* pos_offsets, int32_t fixed_scratch, int64_t* out) {
+  if (num_sms < 1 || B < 1 || B > kMaxBatch || T < 1 || S < 1 || !pos_offsets || !out)
+    return DS4IDX_ERR_INVALID_ARG;
+  int64_t max_vis = 0;
+  for (int b = 0; b < B; ++b) {
+    if (pos_offsets[b] < 0) return DS4IDX_ERR_INVALID_ARG;
+    max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
+  }
+  const Plan pl = fixed_scratch ? make_plan(num_sms, B, T, max_vis, kNoAllocListWords,
+                                            kNoAllocTickets)
+                                : make_plan(num_sms, B, T, max_vis);
+  out[0] = pl.nq;
+  out[1] = pl.n_qb;
+  out[2] = pl.n_splits;
+  out[3] = pl.tiles_per_split;
+  out[4] = pl.grid;
+  out[5] = static_cast<int64_t>(plan_partial_words(pl, B, T));
+  out[6] = static_cast<int64_t>(plan_counters(pl, B));
+  return DS4IDX_OK;
+}
+
 int ds4idx_destroy(ds4idx_t h) {
   if (!h) return DS4IDX_OK;
   const cudaError_t e = cudaDeviceSynchronize();
@@ -387,9 +512,6 @@ int ds4idx_destroy(ds4idx_t h) {
 // array compiled into the library instead of a handle's workspace. See the header for the rules.
 namespace {
 
-constexpr size_t kNoAllocListWords = static_cast<size_t>(1) << 21;  // 16 MiB of list words
-
-constexpr size_t kNoAllocTickets = 4096;  // split tickets, one per query block of a split plan
 // [0, kNoAllocListWords): per-split candidate lists; then the error word (own 256-byte line);
 // then the split tickets (32-bit, zeroed at every call together with the error word).
 static __device__ __align__(256) uint64_t
@@ -458,35 +580,29 @@ extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const
   if (st != DS4IDX_OK) return st;
   const NoAllocDevice& d = g_noalloc_dev[dev];
 
-  int64_t max_vis = 0;
-  for (int b = 0; b < B; ++b) {
-    if (pos_offsets[b] < 0 || pos_offsets[b] > (1LL << 40)) return DS4IDX_ERR_INVALID_ARG;
-    max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
-  }
-  const Plan pl = make_plan(d.num_sms, B, T, max_vis);
-  if (plan_partial_words(pl, B, T) > kNoAllocListWords || plan_counters(pl, B) > kNoAllocTickets)
-    return DS4IDX_ERR_SCRATCH_LIMIT;
-
-  // A stack handle that borrows the fixed scratch; the shared launch path does the rest.
-  ds4idx_handle h;
-  h.cfg.n_heads = kHeads;
-  h.cfg.head_dim = kDim;
-  h.cfg.topk = kTopK;
-  h.cfg.dtype = dtype;
-  h.cfg.max_T = T;
-  h.cfg.max_S = S;
-  h.cfg.max_batch = kMaxBatch;
-  h.device = dev;
-  h.num_sms = d.num_sms;
-  h.partial = d.scratch;
-  h.partial_words = kNoAllocListWords;
-  h.err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords);
-  h.counters = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords + 32);
-  h.n_counters = kNoAllocTickets;
-  // The array keeps the previous call's contents: clear the error word and the tickets.
-  if (cudaMemsetAsync(h.err, 0, 256 + kNoAllocTickets * sizeof(uint32_t),
+  // The shared launch path over the fixed scratch. Short sequences split their key range only
+  // as far as the split lists fit the array (one split uses no list at all).
+  Ctx c;
+  c.dtype = dtype;
+  c.max_T = T;
+  c.max_S = S;
+  c.max_batch = kMaxBatch;
+  c.device = dev;
+  c.num_sms = d.num_sms;
+  c.partial = d.scratch;
+  c.partial_words = kNoAllocListWords;
+  c.err = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords);
+  c.counters = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords + 32);
+  c.n_counters = kNoAllocTickets;
+  c.cap_splits = true;
+  Call call;
+  const int vs = prepare(c, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
+                         nullptr, &call);
+  if (vs != DS4IDX_OK) return vs;
+  // Valid call: the array keeps the previous call's contents, so clear the error word and the
+  // tickets on the stream right before the launch.
+  if (cudaMemsetAsync(c.err, 0, 256 + kNoAllocTickets * sizeof(uint32_t),
                       static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return DS4IDX_ERR_LAUNCH;
-  return run(&h, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score, nullptr,
-             stream);
+  return enqueue(c, call, stream);
 }

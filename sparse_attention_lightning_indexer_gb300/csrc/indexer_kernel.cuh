@@ -95,6 +95,8 @@ struct KParams {
   uint32_t* counters;    // [B * n_qb] split tickets (zero between calls) when n_splits > 1
   float* dense;          // [T, S] scores (debug variant)
   uint32_t* err;         // device error word
+  uint64_t wait_ns;      // limit of one bounded mbarrier wait (kWaitLimitNs)
+  int32_t withhold;      // test only: CTA 0's first selector withholds its first ring release
   int64_t T, S;
   int32_t B, n_qb, n_splits, tiles_per_split;
   int64_t pos[kMaxBatch];
@@ -551,7 +553,8 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
     for (int i = lane; i < ns; i += 32)
       bulk_load(buf + i * kHead, slots + static_cast<int64_t>(i) * kSlotWords, kHead * 8, gbar);
   }
-  if (!mbar_wait(gbar, 0u, abort_flag, p.err)) {
+  // CTA-uniform outcome: a thread may see the copies land while another gives up.
+  if (!__syncthreads_and(mbar_wait(gbar, 0u, abort_flag, p.err, p.wait_ns))) {
     mbar_drain(gbar, 0u);  // never exit with copies in flight
     return;
   }
@@ -641,7 +644,7 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
                     sz * 8u, gbar);
       }
     }
-    if (!mbar_wait(gbar, 1u, abort_flag, p.err)) {
+    if (!__syncthreads_and(mbar_wait(gbar, 1u, abort_flag, p.err, p.wait_ns))) {
       mbar_drain(gbar, 1u);
       return;
     }
@@ -859,7 +862,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       for (; it < n_tiles; ++it) {
         const int st = it % C::kStages;
         const uint32_t ph = (it / C::kStages) & 1;
-        if (!mbar_wait<C::kWaitHint>(&empty[st], ph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait<C::kWaitHint>(&empty[st], ph ^ 1u, s_abort, p.err, p.wait_ns)) break;
         mbar_arrive_expect_tx(&full[st], C::kKBytes);
         uint8_t* dst = sK + st * C::kKBytes;
         const int32_t key0 = (tile_lo + it) * kTileKeys;
@@ -867,25 +870,27 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
           tma_load_3d(dst + h * (kTileKeys * 128), &tmap_k, &full[st],
                       h * 64 * (DT == kDtBf16 ? 1 : 2), key0, b);
       }
-      // Never leave the CTA with copies in flight: wait (bounded) for the last load of each
-      // stage and for the Q block. After a normal run these have long completed.
+      // Never leave the CTA with copies in flight: wait for the last load of each stage and
+      // for the Q block, also after an abort (the waits ignore the abort flag; the copies
+      // complete on their own, the limit only bounds the wait). After a normal run these have
+      // long completed.
       const int issued = it;
       for (int j = issued - C::kStages > 0 ? issued - C::kStages : 0; j < issued; ++j)
-        mbar_wait<C::kWaitHint>(&full[j % C::kStages], (j / C::kStages) & 1, s_abort, p.err);
-      mbar_wait<C::kWaitHint>(qfull, 0, s_abort, p.err);
+        mbar_drain(&full[j % C::kStages], (j / C::kStages) & 1);
+      mbar_drain(qfull, 0);
     }
   } else if (warp == C::kMmaWarp) {
     // ================= MMA issuer (one thread)
     if (lane == 0 && n_tiles > 0) {
       int it = 0;
-      bool ok = mbar_wait<C::kWaitHint>(qfull, 0, s_abort, p.err);
+      bool ok = mbar_wait<C::kWaitHint>(qfull, 0, s_abort, p.err, p.wait_ns);
       for (; ok && it < n_tiles; ++it) {
         const int st = it % C::kStages;
         const uint32_t sph = (it / C::kStages) & 1;
         const int acc = it % C::kAccBufs;
         const uint32_t aph = (it / C::kAccBufs) & 1;
-        if (!mbar_wait<C::kWaitHint>(&full[st], sph, s_abort, p.err)) break;
-        if (!mbar_wait<C::kWaitHint>(&tempty[acc], aph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait<C::kWaitHint>(&full[st], sph, s_abort, p.err, p.wait_ns)) break;
+        if (!mbar_wait<C::kWaitHint>(&tempty[acc], aph ^ 1u, s_abort, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>(acc * C::kN);
         const uint32_t a_base = smem_u32(sK + st * C::kKBytes);
@@ -905,10 +910,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         mma_commit(&tfull[acc]);
       }
       // Before TMEM is released every issued MMA must have completed: wait for the commit of
-      // the last tile issued (the epilogue waits on the same phase).
+      // the last tile issued (the epilogue waits on the same phase), also after an abort.
       if (it > 0) {
         const int last = it - 1;
-        mbar_wait<C::kWaitHint>(&tfull[last % C::kAccBufs], (last / C::kAccBufs) & 1, s_abort, p.err);
+        mbar_drain(&tfull[last % C::kAccBufs], (last / C::kAccBufs) & 1);
       }
     }
     __syncwarp();
@@ -946,10 +951,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         ks_next0 = ks_next1;
         ks_next1 = load_scale(it + 2 * step);
       }
-      if (!mbar_wait_warp<C::kWaitHint>(&tfull[acc], aph, s_abort, p.err)) break;
+      if (!mbar_wait_warp<C::kWaitHint>(&tfull[acc], aph, s_abort, p.err, p.wait_ns)) break;
       tc_fence_after();
       if (!DENSE && !buffered) {
-        if (!mbar_wait_warp<C::kWaitHint>(&sempty[sb], sph ^ 1u, s_abort, p.err)) break;
+        if (!mbar_wait_warp<C::kWaitHint>(&sempty[sb], sph ^ 1u, s_abort, p.err, p.wait_ns)) break;
       }
       // The warp's TMEM reads are 2 * kQPerGroup chunks of 32 head columns. Chunk c+1 is
       // requested before chunk c is reduced, so each load's latency hides behind arithmetic
@@ -1062,7 +1067,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     for (int it = 0; it < (buffered ? 0 : n_tiles); ++it) {
       const int sb = it % C::kScoreBufs;
       const uint32_t sph = (it / C::kScoreBufs) & 1;
-      if (!mbar_wait_warp<C::kWaitHint>(&sfull[sb], sph, s_abort, p.err)) break;
+      if (!mbar_wait_warp<C::kWaitHint>(&sfull[sb], sph, s_abort, p.err, p.wait_ns)) break;
       uint64_t th = theta;
 #pragma unroll
       for (int o = 0; o < C::kSelPerQuery; ++o) th = umax64(th, s_theta[q * C::kSelPerQuery + o]);
@@ -1083,7 +1088,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         n += __popc(m[r]);
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sempty[sb]);
+      // (p.withhold: a test makes the epilogue's bounded wait for this ring slot run out.)
+      if (lane == 0 && !(p.withhold && blockIdx.x == 0 && sidx == 0 && it == 0))
+        mbar_arrive(&sempty[sb]);
       if (n > C::kPool - C::kGroupsPerSel * 32) {
         theta = select_compact<kTopK>(pool, n, hist, lane);
         n = kTopK;

@@ -76,18 +76,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
 // Waits for the phase with the given parity to complete. Gives up (returns false) when the
-// CTA-wide abort flag is raised or after kWaitLimitNs, in which case it raises the flag and
-// records the timeout in the global error word.
+// CTA-wide abort flag is raised or after limit_ns, in which case it raises the flag and records
+// the timeout in the global error word.
 template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile uint32_t* abort_flag, uint32_t* err) {
+                                          volatile uint32_t* abort_flag, uint32_t* err,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait<kHintNs>(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait<kHintNs>(bar, parity)) return true;
     if ((i & 63u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *abort_flag = 1u;
         atomicOr(err, 1u);
         return false;
@@ -100,8 +101,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 // made warp-uniform so callers can branch without divergence.
 template <uint32_t kHintNs = 0>
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity,
-                                               volatile uint32_t* abort_flag, uint32_t* err) {
-  const bool ok = mbar_wait<kHintNs>(bar, parity, abort_flag, err);
+                                               volatile uint32_t* abort_flag, uint32_t* err,
+                                               uint64_t limit_ns = kWaitLimitNs) {
+  const bool ok = mbar_wait<kHintNs>(bar, parity, abort_flag, err, limit_ns);
   return __all_sync(0xffffffffu, ok) != 0;
 }
 
@@ -139,8 +141,9 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
-// Waits (at most kWaitLimitNs, ignoring the abort flag) for copies this CTA still has in flight
-// before it exits after an error.
+// Waits (at most kWaitLimitNs, ignoring the abort flag) for asynchronous work this CTA still
+// has in flight (TMA copies, tensor-core MMAs and their commits) before it frees its tensor
+// memory or exits, also after another warp gave up.
 __device__ __forceinline__ void mbar_drain(uint64_t* bar, uint32_t parity) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity)) {

@@ -17,6 +17,7 @@ from . import build as _build
 
 BF16 = 0
 FP8_E4M3 = 1
+F32 = 2
 H_I = 64
 D_I = 128
 TOPK = 512
@@ -33,7 +34,8 @@ ERR_SCRATCH_LIMIT = -7
 EXPORTS = ("ds4idx_create", "ds4idx_score_topk", "ds4idx_score_topk_batched",
            "ds4idx_score_dense_debug", "ds4idx_sync_status", "ds4idx_destroy",
            "ds4idx_status_string", "ds4idx_version", "ds4idx_score_topk_batched_noalloc",
-           "ds4idx_kernels_launched")
+           "ds4idx_kernels_launched", "ds4idx_debug_wait_test", "ds4idx_plan_query",
+           "ds4idx_quantize_keys", "ds4idx_quantize_queries")
 
 _lock = threading.Lock()
 _lib = None
@@ -89,6 +91,14 @@ def load(path: str | None = None):
         lib.ds4idx_score_topk_batched_noalloc.restype = ctypes.c_int
         lib.ds4idx_kernels_launched.argtypes = []
         lib.ds4idx_kernels_launched.restype = ctypes.c_uint64
+        lib.ds4idx_debug_wait_test.argtypes = [vp, ctypes.c_uint64, i32]
+        lib.ds4idx_debug_wait_test.restype = ctypes.c_int
+        lib.ds4idx_plan_query.argtypes = [i32, i32, i64, i64, vp, i32, vp]
+        lib.ds4idx_plan_query.restype = ctypes.c_int
+        lib.ds4idx_quantize_keys.argtypes = [vp, i32, i64, vp, i64, vp, vp, i64, vp]
+        lib.ds4idx_quantize_keys.restype = ctypes.c_int
+        lib.ds4idx_quantize_queries.argtypes = [vp, i32, i64, vp, vp, vp, vp, vp]
+        lib.ds4idx_quantize_queries.restype = ctypes.c_int
         if path is None:
             _lib = lib
         return lib
@@ -97,6 +107,66 @@ def load(path: str | None = None):
 def kernels_launched() -> int:
     """Kernels the library has enqueued in this process (its own count, for benchmarks)."""
     return int(load().ds4idx_kernels_launched())
+
+
+PLAN_FIELDS = ("queries_per_cta", "query_blocks", "splits", "tiles_per_split", "grid",
+               "list_words", "tickets")
+
+
+def plan_query(num_sms: int, B: int, T: int, S: int, pos_offsets, fixed_scratch: bool = False):
+    """The work decomposition of a call (host computation only): a dict of PLAN_FIELDS."""
+    pos = (ctypes.c_int64 * B)(*[int(x) for x in pos_offsets])
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(load().ds4idx_plan_query(num_sms, B, T, S, ctypes.cast(pos, ctypes.c_void_p),
+                                    1 if fixed_scratch else 0, ctypes.cast(out, ctypes.c_void_p)),
+           "ds4idx_plan_query")
+    return dict(zip(PLAN_FIELDS, list(out)))
+
+
+def _in_dtype(t: torch.Tensor, name: str) -> int:
+    if t.dtype == torch.float32:
+        return F32
+    if t.dtype == torch.bfloat16:
+        return BF16
+    raise TypeError(f"{name} must be float32 or bfloat16")
+
+
+def quantize_keys(k, kcache, kscale, dst_offset: int = 0, slots=None, stream=None):
+    """Writes k [n, 128] (fp32/bf16) as E4M3 codes + scales into kcache [R, 128] uint8 /
+    kscale [R] fp32, at rows dst_offset.. or at slots [n] (int64, -1 skips a row)."""
+    n = k.shape[0]
+    _need(k, (n, D_I), "k")
+    R = kcache.shape[0]
+    _need(kcache, (R, D_I), "kcache", torch.uint8)
+    _need(kscale, (R,), "kscale", torch.float32)
+    if slots is not None:
+        _need(slots, (n,), "slots", torch.int64)
+    _check(load().ds4idx_quantize_keys(_ptr(k), _in_dtype(k, "k"), n, _ptr(slots),
+                                       int(dst_offset), _ptr(kcache), _ptr(kscale), R,
+                                       _stream_ptr(stream)), "ds4idx_quantize_keys")
+    return kcache, kscale
+
+
+def quantize_queries(q, w, q_codes=None, w_out=None, qscale=None, stream=None):
+    """q [T, 64, 128] (fp32/bf16), w [T, 64] -> (E4M3 codes [T, 64, 128] uint8, w' [T, 64],
+    qscale [T])."""
+    T = q.shape[0]
+    _need(q, (T, H_I, D_I), "q")
+    _need(w, (T, H_I), "w", torch.float32)
+    dev = q.device
+    if q_codes is None:
+        q_codes = torch.empty((T, H_I, D_I), dtype=torch.uint8, device=dev)
+    if w_out is None:
+        w_out = torch.empty((T, H_I), dtype=torch.float32, device=dev)
+    if qscale is None:
+        qscale = torch.empty((T,), dtype=torch.float32, device=dev)
+    _need(q_codes, (T, H_I, D_I), "q_codes", torch.uint8)
+    _need(w_out, (T, H_I), "w_out", torch.float32)
+    _need(qscale, (T,), "qscale", torch.float32)
+    _check(load().ds4idx_quantize_queries(_ptr(q), _in_dtype(q, "q"), T, _ptr(w), _ptr(q_codes),
+                                          _ptr(w_out), _ptr(qscale), _stream_ptr(stream)),
+           "ds4idx_quantize_queries")
+    return q_codes, w_out, qscale
 
 
 def status_string(status: int) -> str:
@@ -249,6 +319,11 @@ class Indexer:
                                                 _stream_ptr(stream))
         _check(st, "ds4idx_score_dense_debug")
         return out
+
+    def debug_wait_test(self, wait_limit_ns: int = 2_000_000_000, withhold: bool = False):
+        """Test support: bounded-wait limit for later calls, and one withheld arrival."""
+        _check(self._lib.ds4idx_debug_wait_test(self._h, int(wait_limit_ns), 1 if withhold else 0),
+               "ds4idx_debug_wait_test")
 
     def sync_status(self, stream=None):
         _check(self._lib.ds4idx_sync_status(self._h, _stream_ptr(stream)), "ds4idx_sync_status")

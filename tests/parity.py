@@ -10,8 +10,8 @@ Acceptance rules, per query row t with m = min(topk, visible keys):
   * selection rerun: the oracle's selection step applied to the kernel's own fp32 scores (the
     dense debug export of the same kernel template) reproduces the emitted indices exactly, and
     the emitted scores equal those fp32 scores bit for bit.
-The FP8 tolerance is wide compared with the score spread, so for FP8 a strict set check at
-1e-4 is also computed and reported (not gated).
+The FP8 tolerance is wide compared with the score spread, so the set rule is also applied at
+1e-4 for FP8 (the strict set check, gated by default).
 """
 from __future__ import annotations
 
@@ -40,9 +40,14 @@ def oracle_rows(prob, rows):
     return sc, idx, val
 
 
-def check_rows(prob, rows, gpu_idx, gpu_score, oracle=None, eps=None, strict_eps=1e-4):
+def check_rows(prob, rows, gpu_idx, gpu_score, oracle=None, eps=None, strict_eps=1e-4,
+               gate_strict=True):
     """Applies the score, set and order rules. gpu_* are numpy [len(rows), topk].
 
+    With gate_strict, the set rule is also applied at strict_eps (1e-4) for FP8: the oracle and
+    the kernel decode the same E4M3 codes, so the kernel's only error is fp32 accumulation,
+    far below 1e-4 * (1 + |tau|); a key that leaves the set at that distance from the cut is a
+    real mistake even though the wider FP8 band would admit it.
     Returns a dict of statistics; raises AssertionError with a description on a violation.
     """
     eps = EPS[prob.dtype] if eps is None else eps
@@ -70,10 +75,11 @@ def check_rows(prob, rows, gpu_idx, gpu_score, oracle=None, eps=None, strict_eps
                                    float((err / (1.0 + np.abs(ref))).max(initial=0.0)))
         # order: by emitted score desc, then index asc
         g = gs[:m].astype(np.float64)
-        for a in range(m - 1):
-            if not (g[a] > g[a + 1] or (g[a] == g[a + 1] and sel[a] < sel[a + 1])):
-                raise AssertionError(f"row {t}: emitted list not in (score desc, idx asc) order "
-                                     f"at slot {a}")
+        ordered = (g[:-1] > g[1:]) | ((g[:-1] == g[1:]) & (sel[:-1] < sel[1:]))
+        if not np.all(ordered):
+            a = int(np.nonzero(~ordered)[0][0])
+            raise AssertionError(f"row {t}: emitted list not in (score desc, idx asc) order "
+                                 f"at slot {a}")
         # set rule
         oset = oidx[r, :m]
         assert np.all(oidx[r, m:] == -1)
@@ -89,6 +95,10 @@ def check_rows(prob, rows, gpu_idx, gpu_score, oracle=None, eps=None, strict_eps
         if diff.size:
             stats["strict_set_diff"] += int(
                 (np.abs(sc[r, diff] - tau) > strict_eps * (1.0 + abs(tau))).sum())
+    if gate_strict:
+        assert stats["strict_set_diff"] == 0, (
+            f"{stats['strict_set_diff']} keys differ from the oracle set by more than "
+            f"{strict_eps} * (1 + |tau|) from the cut: {stats}")
     return stats
 
 
@@ -128,3 +138,23 @@ def dense_for_rows(indexer, prob, dev_inputs, rows):
         for r, t in members:
             out[r] = d[t - t0]
     return out
+
+
+def planted_hit_rate(prob, oracle_sets):
+    """Fraction of the visible same-topic planted keys that are in the given Top-k sets of the
+    planted queries. oracle_sets: {query row t: index array}. Returns (rate, number of keys)."""
+    q_rows = prob.meta["planted_queries"].tolist()
+    q_topic = prob.meta["planted_query_topic"].tolist()
+    k_pos = prob.meta["planted_keys"].numpy()
+    k_topic = prob.meta["planted_key_topic"].numpy()
+    hits = total = 0
+    for t, m in zip(q_rows, q_topic):
+        if t not in oracle_sets:
+            continue
+        same = k_pos[(k_topic == m) & (k_pos < prob.n_visible(t))]
+        if same.size == 0:
+            continue
+        chosen = set(int(x) for x in oracle_sets[t] if x >= 0)
+        hits += sum(1 for s in same.tolist() if s in chosen)
+        total += int(same.size)
+    return (hits / total if total else 0.0), total

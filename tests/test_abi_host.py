@@ -43,7 +43,7 @@ def test_status_strings_and_version(lib):
         s = lib.ds4idx_status_string(code).decode()
         assert s and s != "unknown status", code
     assert lib.ds4idx_status_string(-99).decode() == "unknown status"
-    assert lib.ds4idx_version() == (1 << 16)
+    assert lib.ds4idx_version() == (1 << 16) | 1
     assert lib.ds4idx_kernels_launched() == 0  # nothing launched without a device
 
 
@@ -98,3 +98,53 @@ def test_null_handle_and_bad_arguments(lib):
 def test_binding_fails_loudly_without_the_library(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         ds4idx.load(str(tmp_path / "missing.so"))
+
+
+# ---- work decomposition (host arithmetic only, for the 152-SM GB300)
+
+def _plan(lib, B, T, S, pos, fixed=False, sms=152):
+    return ds4idx.plan_query(sms, B, T, S, pos, fixed_scratch=fixed)
+
+
+def test_plans_of_the_workloads(lib):
+    p = _plan(lib, 1, 65536, 65536, [0])  # prefill: query blocks alone fill the GPU
+    assert (p["queries_per_cta"], p["query_blocks"], p["splits"], p["grid"]) == (4, 16384, 1, 16384)
+    assert p["list_words"] == 0 and p["tickets"] == 0
+    p = _plan(lib, 8, 1, 262144, [262143] * 8)  # decode: 19 splits x 8 sequences = one wave
+    assert (p["queries_per_cta"], p["splits"], p["grid"]) == (1, 19, 152)
+    assert p["list_words"] == 8 * 19 * 1152 and p["tickets"] == 8
+    p = _plan(lib, 1, 2048, 262144, [260096])  # the 2048-token chunk: two splits
+    assert (p["splits"], p["grid"], p["list_words"]) == (2, 1024, 1 << 21)
+
+
+def test_fixed_scratch_plans_fit_and_match_when_possible(lib):
+    # The handle plan splits a 768-token chunk further than the fixed array holds.
+    h = _plan(lib, 1, 768, 262144, [262144 - 768])
+    assert h["list_words"] > 1 << 21
+    f = _plan(lib, 1, 768, 262144, [262144 - 768], fixed=True)
+    assert 1 < f["splits"] < h["splits"] and f["list_words"] <= 1 << 21
+    # Where the handle plan fits, the fixed-scratch plan is the same plan.
+    for args in ((8, 1, 262144, [262143] * 8), (1, 2048, 262144, [260096]),
+                 (4, 6, 5000, [4994, 1200, 0, 7])):
+        assert _plan(lib, *args) == _plan(lib, *args, fixed=True)
+    # Every fixed-scratch plan fits, whatever the shape.
+    for B in (1, 2, 8, 64):
+        for T in (1, 2, 5, 64, 700, 1100, 2100, 4096):
+            for S in (1, 600, 9000, 262144, 1 << 20, (1 << 31) - 1):
+                pos = [max(0, S - T)] * B
+                f = _plan(lib, B, T, S, pos, fixed=True)
+                assert f["list_words"] <= 1 << 21 and f["tickets"] <= 4096, (B, T, S, f)
+                assert f["grid"] == B * f["query_blocks"] * f["splits"]
+
+
+def test_plan_query_rejects_bad_arguments(lib):
+    out = (ctypes.c_int64 * 7)()
+    pos = (ctypes.c_int64 * 1)(0)
+    p = ctypes.cast(pos, ctypes.c_void_p)
+    o = ctypes.cast(out, ctypes.c_void_p)
+    assert lib.ds4idx_plan_query(0, 1, 1, 16, p, 0, o) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_plan_query(152, 65, 1, 16, p, 0, o) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_plan_query(152, 1, 0, 16, p, 0, o) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_plan_query(152, 1, 1, 16, None, 0, o) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_plan_query(152, 1, 1, 16, p, 0, None) == ds4idx.ERR_INVALID_ARG
+    assert lib.ds4idx_debug_wait_test(None, 2000000000, 0) == ds4idx.ERR_INVALID_ARG

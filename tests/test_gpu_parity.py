@@ -281,3 +281,48 @@ def test_single_query_clipped_windows(fp8_ix):
     stats, gi, _ = run_full(prob, fp8_ix)
     # the scaled keys with a positive score (about half) lead the row
     assert len(set(pick.tolist()) & set(gi[0, :40].tolist())) >= 10
+
+
+# ---- cases where the relative tolerance bites: scores far above 1
+
+W_GAIN = 2.0 ** 12  # exact in fp32; I is positively homogeneous in w, so |I| grows to ~40
+
+
+@pytest.mark.parametrize("dtype", [inputs.FP8_E4M3, inputs.BF16])
+@pytest.mark.parametrize("T,S,pos", [(1001, 1001, 0), (300, 2000, 1700), (7, 5000, 2000),
+                                     (1, 9000, 8999)])
+def test_large_scores_relative_tolerance(dtype, T, S, pos, bf16_ix, fp8_ix):
+    # With w scaled by 2^12 the scores reach tens, so eps * (1 + |I|) is a relative bound
+    # (2% for FP8, 1e-4 for bf16) and the strict 1e-4 set rule is a relative check of the cut.
+    # T > 1 runs the four-query kernel (ragged key tiles and query blocks, pos_offset > 0, a
+    # split plan for T = 7); T = 1 the one-query kernel with its split merge.
+    prob = inputs.make("big", T=T, S=S, pos_offset=pos, seed=70 + T, dtype=dtype)
+    prob.w.mul_(W_GAIN)
+    stats, _, gs = run_full(prob, _ix(prob, bf16_ix, fp8_ix))
+    assert np.abs(gs[np.isfinite(gs)]).max() > 10.0  # the scale really is large
+    assert stats["strict_set_diff"] == 0
+    # fp32 accumulation of exactly decoded operands: far inside both tolerances (measured on
+    # GB300: below 6e-6 for FP8, 1.6e-5 for bf16, whose tensor-core sums carry more terms)
+    assert stats["max_rel_err"] < 5e-5, stats
+    print(dtype, T, S, pos, stats)
+
+
+# ---- bounded device waits: a lost arrival becomes DEVICE_TIMEOUT, not a hang
+
+def test_device_timeout_is_reported_and_the_next_call_is_exact():
+    # T = S = 4096: 1024 query blocks, no key split; the first CTA (the last queries) runs 32 key
+    # tiles, so its score ring (28 tiles) wraps and the epilogue waits for the withheld release.
+    prob = inputs.make("timeout", T=4096, S=4096, pos_offset=0, seed=80, dtype=inputs.BF16)
+    with ds4idx.Indexer(ds4idx.BF16, max_T=4096, max_S=4096) as ix:
+        dev = parity.to_device(prob)
+        ix.debug_wait_test(1_000_000, withhold=True)  # 1 ms limit
+        ix.score_topk(*dev, pos_offset=0)
+        with pytest.raises(ds4idx.Ds4IdxError) as e:
+            ix.sync_status()
+        assert e.value.status == ds4idx.ERR_DEVICE_TIMEOUT
+        ix.debug_wait_test(2_000_000_000, withhold=False)
+        idx, sc = ix.score_topk(*dev, pos_offset=0)
+        ix.sync_status()  # the error word was cleared: the normal call reports OK
+        rows = inputs.sample_rows(prob.T, 80, n_random=128)
+        stats = parity.check_rows(prob, rows, idx[rows].cpu().numpy(), sc[rows].cpu().numpy())
+        assert stats["rows"] == len(rows)
