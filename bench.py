@@ -453,12 +453,276 @@ def run_ours(args, rank, world, local_rank):
     ix.close()
 
 
+# The FP8 index-cache writer over the 128k FP8 workload: one step quantises its 131072 query
+# tokens (bf16 in, one scale per token, folded into w) and its 131072 new keys (bf16 in).
+WRITER_JOBS = {"fp8_cache_write_128k": dict(T=131072, S=131072, seed=3)}
+
+
+def _timed(step, steps, stream, world, dev, local_rank):
+    from sparse_attention_lightning_indexer_gb300 import ds4idx
+    with ClockSampler(local_rank) as clk:
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        launched0 = ds4idx.kernels_launched()
+        ev0.record(stream)
+        for _ in range(steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        launched = ds4idx.kernels_launched() - launched0
+    return ev0.elapsed_time(ev1), launched, clk.summary()
+
+
+def run_writer(args, rank, world, local_rank):
+    """Benchmark of the FP8 index-cache writer (HBM-bound): tokens quantised per second."""
+    from sparse_attention_lightning_indexer_gb300 import ds4idx
+    from sparse_attention_lightning_indexer_gb300 import build as _build
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if world == 1 or rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ds4idx.load()
+    spec = WRITER_JOBS[args.workload]
+    T, S, seed = spec["T"], spec["S"], spec["seed"]
+    qf, kf, wf = inputs.draw_f32(T, S, seed)
+    hq, hk, hw = qf.to(torch.bfloat16), kf.to(torch.bfloat16), wf
+    del qf, kf
+    dev = torch.device("cuda", local_rank)
+    q, k, w = hq.to(dev), hk.to(dev), hw.to(dev)
+    qc = torch.empty((T, inputs.H_I, inputs.D_I), dtype=torch.uint8, device=dev)
+    wo = torch.empty((T, inputs.H_I), dtype=torch.float32, device=dev)
+    qs = torch.empty((T,), dtype=torch.float32, device=dev)
+    kc = torch.empty((S, inputs.D_I), dtype=torch.uint8, device=dev)
+    ks = torch.empty((S,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ds4idx.quantize_queries(q, w, qc, wo, qs, stream=stream)
+        ds4idx.quantize_keys(k, kc, ks, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    total_ms, launched, clocks = _timed(step, args.steps, stream, world, dev, local_rank)
+    units = T + S
+    t_max, value = aggregate(total_ms, units * args.steps, device=dev)
+
+    # end to end: bf16 inputs from pinned host memory, codes, scales and w' back to the host
+    pq, pk, pw = hq.pin_memory(), hk.pin_memory(), hw.pin_memory()
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (qc, wo, qs, kc, ks)]
+    h2d = sum(t.numel() * t.element_size() for t in (pq, pk, pw))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+
+    def e2e_step():
+        q.copy_(pq, non_blocking=True)
+        k.copy_(pk, non_blocking=True)
+        w.copy_(pw, non_blocking=True)
+        step()
+        for h, d in zip(outs, (qc, wo, qs, kc, ks)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps // 2, 20))
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms, _, _ = _timed(e2e_step, e2e_steps, stream, world, dev, local_rank)
+    _, e2e_value = aggregate(e2e_ms, units * e2e_steps, device=dev)
+
+    spot = "skipped"
+    cpu = None
+    if rank == 0:
+        from oracle import oracle as orc
+        rows = np.linspace(0, T - 1, 64).astype(np.int64)
+        c, sc = orc.quantize_rows(hq[rows].float().reshape(len(rows), -1).numpy())
+        ok = np.array_equal(qc[rows].cpu().numpy().reshape(len(rows), -1), c) and \
+            np.array_equal(qs[rows].cpu().numpy(), sc)
+        kr = np.linspace(0, S - 1, 4096).astype(np.int64)
+        c2, s2 = orc.quantize_rows(hk[kr].float().numpy())
+        ok = ok and np.array_equal(kc[kr].cpu().numpy(), c2) and np.array_equal(ks[kr].cpu().numpy(), s2)
+        spot = "64 query tokens and 4096 keys bit-exact with the oracle" if ok else "MISMATCH"
+        if args.cpu_budget > 0:
+            def oracle_tokens(n):  # n query tokens and n keys
+                t0 = time.perf_counter()
+                orc.quantize_rows(hq[:n].float().reshape(n, -1).numpy())
+                orc.quantize_rows(hk[:n].float().numpy())
+                return time.perf_counter() - t0
+            n_tok = 256
+            dt = oracle_tokens(n_tok)
+            n_tok = int(min(T, max(n_tok, n_tok * args.cpu_budget / max(dt, 1e-3))))
+            dt = oracle_tokens(n_tok)
+            cpu = {"value": 2 * n_tok / dt, "unit": "tokens/s", "cores": orc.num_threads(),
+                   "kind": "oracle",
+                   "sample": f"the first {n_tok} query tokens and {n_tok} keys of the workload "
+                             f"(brute-force E4M3 rounding), {dt:.1f} s"}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    avg_ms = total_ms / args.steps
+    moved = float(T * inputs.H_I * inputs.D_I * (2 + 1) + T * inputs.H_I * 4 * 2 + T * 4
+                  + S * inputs.D_I * (2 + 1) + S * 4)
+    achieved = moved / (avg_ms / 1000.0) / 1e9
+    out = {"metric": "FP8 index-cache writer tokens/s (queries + keys quantised) and % of HBM",
+           "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": t_max / args.steps, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "bf16->e4m3", "data": "synthetic",
+           "config": {"workload": args.workload, "T": T, "S": S, "H_I": inputs.H_I,
+                      "d_I": inputs.D_I, "seed": seed,
+                      "l2": "inputs larger than L2 (q is %.0f MiB)" % (q.numel() * 2 / 2**20),
+                      "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+           "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": None,
+                        "peak_source": f"hbm copy bandwidth, {peak_src}",
+                        "algorithmic": f"{moved:.4g} B: bf16 q and k read once, E4M3 codes, "
+                                       f"scales, w read and w' written once",
+                        "timed": "two launches per step (queries, keys); average over K steps"},
+           "cpu_baseline": cpu,
+           "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                   "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+           "gpu_launches": launched, "clocks": clocks, "parity_spot_check": spot}
+    print(json.dumps(out), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# Sparse attention over the indexer's Top-512: the last 4096 query tokens of a 64k-token
+# sequence (indices from an indexer call on those rows), 128 heads over 576-wide latent rows.
+ATTN_JOBS = {"sparse_attn_4k_of_64k": dict(T=4096, S=65536, pos_offset=61440, seed=2)}
+
+
+def run_attention(args, rank, world, local_rank):
+    """Benchmark of sparse attention over the selected keys (tensor-bound): query tokens/s."""
+    from sparse_attention_lightning_indexer_gb300 import ds4idx
+    from sparse_attention_lightning_indexer_gb300 import build as _build
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if world == 1 or rank == 0:
+        _build.build()
+    if world > 1:
+        torch.distributed.barrier()
+    ds4idx.load()
+    spec = ATTN_JOBS[args.workload]
+    T, S, pos, seed = spec["T"], spec["S"], spec["pos_offset"], spec["seed"]
+    dev = torch.device("cuda", local_rank)
+    # the selection: the indexer on these queries (untimed)
+    prob = inputs.make(args.workload, T=T, S=S, pos_offset=pos, seed=seed, dtype=inputs.BF16)
+    with ds4idx.Indexer(inputs.BF16, max_T=T, max_S=S) as ix:
+        idx, _ = ix.score_topk(prob.q.to(dev), prob.w.to(dev), prob.k.to(dev), None, pos)
+        ix.sync_status()
+    g = torch.Generator().manual_seed(seed * 1009 + 11)
+    hq = torch.randn(T, ds4idx.SA_HEADS, ds4idx.SA_DQK, generator=g).to(torch.bfloat16)
+    hkv = torch.randn(S, ds4idx.SA_DQK, generator=g).to(torch.bfloat16)
+    hidx = idx.cpu()
+    q, kv = hq.to(dev), hkv.to(dev)
+    scale = ds4idx.SA_DQK ** -0.5
+    out = torch.empty((T, ds4idx.SA_HEADS, ds4idx.SA_DV), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, ds4idx.SA_HEADS), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ds4idx.sparse_attention(q, kv, idx, scale, out=out, lse=lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    ds4idx.sparse_attention_status()
+    total_ms, launched, clocks = _timed(step, args.steps, stream, world, dev, local_rank)
+    ds4idx.sparse_attention_status()
+    t_max, value = aggregate(total_ms, T * args.steps, device=dev)
+    pq, pkv, pidx = hq.pin_memory(), hkv.pin_memory(), hidx.pin_memory()
+    pout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    plse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (pq, pkv, pidx))
+    d2h = pout.numel() * 2 + plse.numel() * 4
+
+    def e2e_step():
+        q.copy_(pq, non_blocking=True)
+        kv.copy_(pkv, non_blocking=True)
+        idx.copy_(pidx, non_blocking=True)
+        step()
+        pout.copy_(out, non_blocking=True)
+        plse.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, min(args.steps // 2, 20))
+    e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms, _, _ = _timed(e2e_step, e2e_steps, stream, world, dev, local_rank)
+    _, e2e_value = aggregate(e2e_ms, T * e2e_steps, device=dev)
+    spot, cpu = "skipped", None
+    if rank == 0:
+        from oracle import oracle as orc
+        rows = np.linspace(0, T - 1, 8).astype(np.int64)
+        o_ref, l_ref = orc.sparse_attention(hq, hkv, hidx.numpy(), scale, ds4idx.SA_DV, rows=rows)
+        err = float(np.abs(out[rows].float().cpu().numpy() - o_ref).max())
+        lerr = float(np.abs(lse[rows].cpu().numpy() - l_ref).max())
+        spot = f"8 tokens vs the oracle: max |d out| {err:.3g}, max |d lse| {lerr:.3g}"
+        if args.cpu_budget > 0:
+            n = max(1, orc.num_threads())
+            t0 = time.perf_counter()
+            orc.sparse_attention(hq, hkv, hidx.numpy(), scale, ds4idx.SA_DV, rows=np.arange(n))
+            dt = time.perf_counter() - t0
+            n2 = int(min(T, max(n, n * args.cpu_budget / max(dt, 1e-3))))
+            t0 = time.perf_counter()
+            orc.sparse_attention(hq, hkv, hidx.numpy(), scale, ds4idx.SA_DV, rows=np.arange(n2))
+            dt = time.perf_counter() - t0
+            cpu = {"value": n2 / dt, "unit": UNIT, "cores": orc.num_threads(), "kind": "oracle",
+                   "sample": f"first {n2} query tokens (fp64, all 128 heads), {dt:.1f} s"}
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+    peaks, peak_src = load_peaks()
+    avg_ms = total_ms / args.steps
+    valid = int((hidx >= 0).sum())
+    flops = 2.0 * ds4idx.SA_HEADS * valid * (ds4idx.SA_DQK + ds4idx.SA_DV)
+    achieved = flops / (avg_ms / 1000.0) / 1e12
+    out_line = {"metric": "sparse attention query-tokens/s over the Top-512 (128 heads, 576/512 "
+                          "latent) and % of bf16 tensor roofline",
+                "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": t_max / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic",
+                "config": {"workload": args.workload, "T": T, "S": S, "pos_offset": pos,
+                           "heads": ds4idx.SA_HEADS, "d_qk": ds4idx.SA_DQK, "d_v": ds4idx.SA_DV,
+                           "topk": 512, "seed": seed,
+                           "l2": "q is %.0f MiB (larger than L2); the 72 MiB latent cache fits "
+                                 "L2" % (q.numel() * 2 / 2**20),
+                           "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                "roofline": {"bound": "tensor", "achieved": achieved,
+                             "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                             "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                             "peak_source": f"bf16 dense, {peak_src} (burst)",
+                             "algorithmic": f"{flops:.4g} flop = 2*128*(576+512) * {valid} "
+                                            f"selected (token, key) pairs",
+                             "timed": "one launch per step; average over K steps"},
+                "cpu_baseline": cpu,
+                "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                        "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+                "gpu_launches": launched, "clocks": clocks, "parity_spot_check": spot}
+    print(json.dumps(out_line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=30)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="prefill_64k", choices=JOBS)
+    ap.add_argument("--workload", default="prefill_64k",
+                    choices=JOBS + sorted(WRITER_JOBS) + sorted(ATTN_JOBS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle time for cpu_baseline (0 disables)")
@@ -480,6 +744,10 @@ def main():
         sys.exit(2)
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload in WRITER_JOBS:
+        run_writer(args, rank, world, local_rank)
+    elif args.workload in ATTN_JOBS:
+        run_attention(args, rank, world, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
 

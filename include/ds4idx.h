@@ -108,6 +108,38 @@ int ds4idx_score_topk_batched(ds4idx_t h, int32_t B, const void* q, const float*
                               const int64_t* pos_offsets, int32_t topk, int32_t* out_idx,
                               float* out_score, void* stream);
 
+/* Variable-length, optionally paged batch: B independent sequences, each with its own number
+ * of queries, its own key count and its own position, in one launch (continuous-batching decode
+ * and mixed chunked prefill). The pages have no interface for this; the concurrency sweep and
+ * the hybrid KV-cache rows of "DeepSeek V4 Flash는 단일 AMD MI300X에서 실행됩니다" (동시성 스윕,
+ * 프로덕션 수준 튜닝 세부 사항) are the serving setting it is for.
+ *  q, w          packed queries of all sequences: q [Q, 64, 128], w [Q, 64] fp32, where
+ *                Q = cu_seqlens_q[B]; sequence b owns rows cu_seqlens_q[b] .. cu_seqlens_q[b+1]-1
+ *                (cu_seqlens_q: HOST int64 [B + 1], starting at 0, non-decreasing; a sequence
+ *                may have no query).
+ *  kcache        the key pool [pool_rows, 128] (bf16 or E4M3 codes), pool_rows < 2^31;
+ *  kscale        [pool_rows] fp32 for FP8 handles, NULL for bf16.
+ *  Keys of sequence b (S_b = seq_lens[b] >= 1, HOST int64 [B]) are found either
+ *   - contiguously: kv_start (HOST int64 [B]) gives the pool row of its key 0, or
+ *   - through a page table: page_table (DEVICE int32 [B, pages_per_seq], 4-byte aligned) lists
+ *     the pages of sequence b in key order; page_size keys per page (a multiple of 64); key s
+ *     lives in pool row page_table[b][s / page_size] * page_size + s % page_size. Page ids are
+ *     not checked on the host: an id outside the pool reads as zero keys (wrong results, no
+ *     out-of-bounds access).
+ *    Exactly one of kv_start and page_table is given.
+ *  pos_offsets   HOST int64 [B]: the position of each sequence's first query (as in
+ *                ds4idx_score_topk: query t sees keys 0 .. min(pos + t, S_b - 1)).
+ *  out_idx / out_score  [Q, topk], rows packed like q. Key indices are positions within the
+ *                sequence (0 .. S_b - 1), not pool rows.
+ * Limits: B <= max_batch, every T_b <= max_T and S_b <= max_S of the handle. Key-range splits of
+ * short sequences are fitted to the handle's workspace. Errors: INVALID_ARG, LAUNCH, CUDA. */
+int ds4idx_score_topk_varlen(ds4idx_t h, int32_t B, const void* q, const float* w,
+                             const int64_t* cu_seqlens_q, const void* kcache, const float* kscale,
+                             int64_t pool_rows, const int64_t* kv_start,
+                             const int32_t* page_table, int32_t page_size, int32_t pages_per_seq,
+                             const int64_t* seq_lens, const int64_t* pos_offsets, int32_t topk,
+                             int32_t* out_idx, float* out_score, void* stream);
+
 /* Debug/test entry: the fp32 scores the selection kernels see, before selection.
  * out_scores [T, S] fp32, written: I[t,s] for visible s, -inf for s > p(t). Same inputs and
  * rules as ds4idx_score_topk; it runs the same scoring code path. */
@@ -197,6 +229,53 @@ int ds4idx_quantize_keys(const void* k, int32_t in_dtype, int64_t n, const int64
  * LAUNCH. T = 0 is a no-op. */
 int ds4idx_quantize_queries(const void* q, int32_t in_dtype, int64_t T, const float* w,
                             uint8_t* q_codes, float* w_out, float* qscale, void* stream);
+
+/* ---- Merge of key-sharded Top-k lists (the exchange step of a key-range-sharded indexer).
+ * When the keys of a sequence are split into disjoint ranges (shards) and each shard's Top-k is
+ * computed on its own (ds4idx_score_topk on that range), the union of the shards' lists holds
+ * the global Top-k: a key among the k best of all keys is also among the k best of its shard.
+ * This call merges them: for every row it takes the k largest (score, key) pairs of all lists,
+ * ordered by score descending with ties to the lower key, padded with (-1, -inf).
+ *  in_idx, in_score  DEVICE [n_lists, rows, topk] int32 / fp32: each list's indices are local to
+ *                    its shard (-1 = empty slot); 1 <= n_lists <= 16.
+ *  idx_offsets       HOST int64 [n_lists]: the first key of each shard, added to its indices
+ *                    (merged keys must stay below 2^31).
+ *  row0              HOST int64 [n_lists] or NULL: list l has no entries for rows < row0[l]
+ *                    (queries that see none of its keys); NULL = all rows.
+ *  out_idx, out_score DEVICE [rows, topk] (out_score may be NULL). topk must be 512.
+ * Shards must be disjoint (a key in two lists would be kept twice). Asynchronous on `stream`,
+ * allocates nothing. Errors: INVALID_ARG, LAUNCH, CUDA. */
+int ds4idx_merge_topk(int32_t n_lists, int64_t rows, const int32_t* in_idx,
+                      const float* in_score, const int64_t* idx_offsets, const int64_t* row0,
+                      int32_t topk, int32_t* out_idx, float* out_score, void* stream);
+
+/* ---- Sparse attention over the selected keys: the step that consumes the indexer's output.
+ * "DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화", 용어 해설 (희소 어텐션, Lightning Indexer):
+ * sparse attention computes only some token pairs, and the indexer picks the positions. For
+ * query token t and head h over its selected positions J(t) (one row of out_idx; -1 = empty):
+ *     s_j = sm_scale * q[t,h,:] . kv[j,:],   out[t,h,:] = sum_j softmax(s)_j * kv[j, 0:d_v],
+ *     lse[t,h] = log sum_j exp(s_j)          (natural log; -inf and out = 0 if J(t) is empty)
+ * with one latent row per position shared by all heads (the value is the row's first d_v dims).
+ *  q       DEVICE [T, n_heads, d_qk] bf16, 16-byte aligned.
+ *  kv      DEVICE [kv_rows, d_qk] bf16 (1 <= kv_rows < 2^31), 16-byte aligned.
+ *  idx     DEVICE [T, topk] int32: selected positions; position s of token t is kv row
+ *          kv_row0[t] + s (kv_row0: DEVICE int64 [T], or NULL for 0). Positions whose row falls
+ *          outside [0, kv_rows) are treated as empty. Selected positions must be distinct.
+ *  out     DEVICE [T, n_heads, d_v] bf16; lse DEVICE [T, n_heads] fp32 or NULL.
+ * Built shape: n_heads = 128, d_qk = 576, d_v = 512, topk = 512 (else UNSUPPORTED); sm_scale > 0.
+ * Arithmetic: bf16 products with fp32 accumulation on the tensor cores, fp32 softmax, the
+ * probabilities rounded to bf16 for the value product, the output rounded to bf16.
+ * Asynchronous on `stream`, allocates nothing. Bounded device waits that run out are recorded
+ * for ds4idx_sparse_attention_status. Errors: INVALID_ARG, UNSUPPORTED, LAUNCH, CUDA. */
+int ds4idx_sparse_attention(const void* q, const void* kv, int64_t kv_rows, const int32_t* idx,
+                            const int64_t* kv_row0, int64_t T, int32_t n_heads, int32_t d_qk,
+                            int32_t d_v, int32_t topk, float sm_scale, void* out, float* lse,
+                            void* stream);
+
+/* Synchronises `stream`, then reads and clears the sparse-attention error word: DEVICE_TIMEOUT if
+ * a kernel gave up on a bounded wait since the last check (outputs undefined), CUDA if the
+ * synchronisation failed, else OK. */
+int ds4idx_sparse_attention_status(void* stream);
 
 /* Test support for the bounded device waits (the pages have no counterpart). Every mbarrier
  * wait in the kernels gives up after a limit (2 s by default), records DS4IDX_ERR_DEVICE_TIMEOUT

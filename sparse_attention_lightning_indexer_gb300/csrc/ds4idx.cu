@@ -230,109 +230,276 @@ Ctx handle_ctx(const ds4idx_handle* h) {
 
 // A validated call, ready to enqueue.
 struct Call {
-  Plan pl;
+  int nq = 4;
+  int64_t grid = 0;
   CUtensorMap tq, tk;
   KParams kp;
   bool dense = false;
-  bool noop = false;  // T = 0
+  bool noop = false;  // no query at all
 };
+
+// One sequence of a call, as the caller describes it.
+struct SeqSpec {
+  int64_t T = 0, S = 0, pos = 0;
+  int64_t q_row0 = 0;  // first row in the packed q / w / outputs
+  int64_t k_row0 = 0;  // first row in the contiguous key pool (unused when paged)
+};
+
+// Everything a compute call passes, in one place.
+struct CallSpec {
+  int32_t B = 0;
+  SeqSpec seq[kMaxBatch];
+  bool uniform = true;       // every sequence has the same T, S (batched / single calls)
+  int64_t q_rows = 0;        // rows of the packed queries (sum of T)
+  int64_t pool_rows = 0;     // rows of the key pool
+  const void* q = nullptr;
+  const float* w = nullptr;
+  const void* kcache = nullptr;
+  const float* kscale = nullptr;
+  const int32_t* page_table = nullptr;  // device [B, pt_stride], or null (contiguous)
+  int32_t page_size = 0;
+  int32_t pt_stride = 0;
+  int32_t topk = kTopK;
+  int32_t* out_idx = nullptr;
+  float* out_score = nullptr;
+  float* dense = nullptr;
+};
+
+// Split plan for sequences of different lengths: one key-tile count per split for all of them
+// (a sequence gets ceil(its tiles / tps) splits), chosen like the uniform plan: the fewest
+// splits whose estimated wave occupancy is within 5% of the best; then fewer splits until the
+// lists and tickets fit the scratch.
+void plan_varlen(int num_sms, const CallSpec& cs, int nq, size_t max_words, size_t max_tickets,
+                 int32_t* n_qb, int32_t* n_splits, int32_t* tps_out) {
+  int64_t blocks = 0, max_tiles = 1;
+  int64_t tiles[kMaxBatch];
+  for (int b = 0; b < cs.B; ++b) {
+    const SeqSpec& q = cs.seq[b];
+    n_qb[b] = static_cast<int32_t>((q.T + nq - 1) / nq);
+    const int64_t vis = q.T > 0 ? std::min<int64_t>(q.pos + q.T, q.S) : 0;
+    tiles[b] = (vis + kTileKeys - 1) / kTileKeys;
+    blocks += n_qb[b];
+    max_tiles = std::max<int64_t>(max_tiles, tiles[b]);
+  }
+  auto splits_of = [&](int b, int64_t tps) {
+    return static_cast<int32_t>(std::max<int64_t>(1, (tiles[b] + tps - 1) / tps));
+  };
+  auto fits = [&](int64_t tps) {
+    size_t words = 0, tickets = 0;
+    const size_t per = nq == 1 ? static_cast<size_t>(kSlotWords) : static_cast<size_t>(kTopK);
+    for (int b = 0; b < cs.B; ++b) {
+      const int32_t sp = splits_of(b, tps);
+      if (sp > 1) {
+        words += static_cast<size_t>(cs.seq[b].T) * sp * per;
+        tickets += static_cast<size_t>(n_qb[b]);
+      }
+    }
+    return words <= max_words && tickets <= max_tickets;
+  };
+  int64_t tps = max_tiles;  // one split each
+  if (blocks < 4LL * num_sms) {
+    const int64_t max_s = std::min<int64_t>(kMaxSplits, std::max<int64_t>(1, max_tiles / kMinTilesPerSplit));
+    auto occupancy = [&](int64_t t) {  // tile work over the tile slots of the waves it needs
+      int64_t ctas = 0, work = 0;
+      for (int b = 0; b < cs.B; ++b) {
+        ctas += static_cast<int64_t>(n_qb[b]) * splits_of(b, t);
+        work += static_cast<int64_t>(n_qb[b]) * tiles[b];
+      }
+      const int64_t waves = (ctas + num_sms - 1) / num_sms;
+      return static_cast<double>(work) / static_cast<double>(waves * num_sms * t);
+    };
+    double best = 0.0;
+    for (int64_t sp = 1; sp <= max_s; ++sp) best = std::max(best, occupancy((max_tiles + sp - 1) / sp));
+    for (int64_t sp = 1; sp <= max_s; ++sp) {
+      const int64_t t = (max_tiles + sp - 1) / sp;
+      if (occupancy(t) >= best - 0.05) {
+        tps = t;
+        break;
+      }
+    }
+  }
+  while (tps < max_tiles && !fits(tps)) ++tps;
+  for (int b = 0; b < cs.B; ++b) n_splits[b] = splits_of(b, tps);
+  *tps_out = static_cast<int32_t>(tps);
+}
 
 // Validates a compute call and prepares its launch. Enqueues nothing and touches no device
 // memory: every argument error is reported here, before any work is queued.
-int prepare(const Ctx& c, int32_t B, const void* q, const float* w, const void* kcache,
-            const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
-            int32_t* out_idx, float* out_score, float* dense, Call* call) {
-  if (B < 1 || B > c.max_batch || B > kMaxBatch) return DS4IDX_ERR_INVALID_ARG;
-  if (T < 0 || T > c.max_T || S < 1 || S > c.max_S) return DS4IDX_ERR_INVALID_ARG;
-  if (!pos_offsets) return DS4IDX_ERR_INVALID_ARG;
-  if (!dense && topk != kTopK) return DS4IDX_ERR_INVALID_ARG;
-  call->dense = dense != nullptr;
-  call->noop = T == 0;
-  if (T == 0) return DS4IDX_OK;
-  if (!q || !w || !kcache || !aligned16(q) || !aligned16(w) || !aligned16(kcache))
+int prepare(const Ctx& c, const CallSpec& cs, Call* call) {
+  const bool dense = cs.dense != nullptr;
+  if (cs.B < 1 || cs.B > c.max_batch || cs.B > kMaxBatch) return DS4IDX_ERR_INVALID_ARG;
+  if (!dense && cs.topk != kTopK) return DS4IDX_ERR_INVALID_ARG;
+  int64_t total_T = 0;
+  for (int b = 0; b < cs.B; ++b) {
+    const SeqSpec& q = cs.seq[b];
+    if (q.T < 0 || q.T > c.max_T || q.S < 1 || q.S > c.max_S) return DS4IDX_ERR_INVALID_ARG;
+    if (q.pos < 0 || q.pos > (1LL << 40) || q.q_row0 < 0 || q.k_row0 < 0)
+      return DS4IDX_ERR_INVALID_ARG;
+    if (q.T > 0 && q.q_row0 + q.T > cs.q_rows) return DS4IDX_ERR_INVALID_ARG;
+    if (!cs.page_table && q.k_row0 + q.S > cs.pool_rows) return DS4IDX_ERR_INVALID_ARG;
+    if (cs.page_table && (q.S + cs.page_size - 1) / cs.page_size > cs.pt_stride)
+      return DS4IDX_ERR_INVALID_ARG;
+    total_T += q.T;
+  }
+  call->dense = dense;
+  call->noop = total_T == 0;
+  if (call->noop) return DS4IDX_OK;
+  if (cs.q_rows * kHeads > (1LL << 31) - 1 || cs.pool_rows < 1 || cs.pool_rows > (1LL << 31) - 1)
+    return DS4IDX_ERR_INVALID_ARG;
+  if (cs.page_table && (cs.page_size < 64 || cs.page_size % 64 != 0 || cs.pt_stride < 1 ||
+                        (reinterpret_cast<uintptr_t>(cs.page_table) & 3u)))
+    return DS4IDX_ERR_INVALID_ARG;
+  if (!cs.q || !cs.w || !cs.kcache || !aligned16(cs.q) || !aligned16(cs.w) || !aligned16(cs.kcache))
     return DS4IDX_ERR_INVALID_ARG;
   if (c.dtype == DS4IDX_FP8_E4M3) {
-    if (!kscale || (reinterpret_cast<uintptr_t>(kscale) & 3u)) return DS4IDX_ERR_INVALID_ARG;
-  } else if (kscale) {
+    if (!cs.kscale || (reinterpret_cast<uintptr_t>(cs.kscale) & 3u)) return DS4IDX_ERR_INVALID_ARG;
+  } else if (cs.kscale) {
     return DS4IDX_ERR_INVALID_ARG;
   }
   if (dense) {
-    if (!aligned16(dense)) return DS4IDX_ERR_INVALID_ARG;
+    if (!aligned16(cs.dense) || cs.B != 1) return DS4IDX_ERR_INVALID_ARG;
   } else {
-    if (!out_idx || !aligned16(out_idx)) return DS4IDX_ERR_INVALID_ARG;
-    if (out_score && !aligned16(out_score)) return DS4IDX_ERR_INVALID_ARG;
+    if (!cs.out_idx || !aligned16(cs.out_idx)) return DS4IDX_ERR_INVALID_ARG;
+    if (cs.out_score && !aligned16(cs.out_score)) return DS4IDX_ERR_INVALID_ARG;
   }
-  int64_t max_vis = 0;
-  for (int b = 0; b < B; ++b) {
-    if (pos_offsets[b] < 0 || pos_offsets[b] > (1LL << 40)) return DS4IDX_ERR_INVALID_ARG;
-    max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(pos_offsets[b] + T, S));
-  }
-  if (T * kHeads > (1LL << 31) - 1) return DS4IDX_ERR_INVALID_ARG;
   if (!load_encode()) return DS4IDX_ERR_CUDA;
-
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess || cur != c.device) return DS4IDX_ERR_INVALID_ARG;
 
-  Plan pl = c.cap_splits ? make_plan(c.num_sms, B, T, max_vis, c.partial_words, c.n_counters)
-                         : make_plan(c.num_sms, B, T, max_vis);
+  // ---- work decomposition
+  bool all_one = true;
+  for (int b = 0; b < cs.B; ++b) all_one = all_one && cs.seq[b].T <= 1;
+  const int nq = dense ? queries_per_cta(cs.seq[0].T) : (all_one ? 1 : 4);
+  int32_t n_qb[kMaxBatch], n_splits[kMaxBatch];
+  int32_t tps = 0;
   if (dense) {
-    // Same query blocking as the Top-k path, so the debug scores come from identical MMA tiles.
-    pl.nq = queries_per_cta(T);
-    pl.n_qb = static_cast<int>((T + pl.nq - 1) / pl.nq);
-    pl.n_splits = 1;
-    pl.tiles_per_split = static_cast<int>((S + kTileKeys - 1) / kTileKeys);
-    pl.grid = pl.n_qb;
+    n_qb[0] = static_cast<int32_t>((cs.seq[0].T + nq - 1) / nq);
+    n_splits[0] = 1;
+    tps = static_cast<int32_t>((cs.seq[0].S + kTileKeys - 1) / kTileKeys);
+  } else if (cs.uniform) {
+    int64_t max_vis = 0;
+    for (int b = 0; b < cs.B; ++b)
+      max_vis = std::max<int64_t>(max_vis, std::min<int64_t>(cs.seq[b].pos + cs.seq[0].T, cs.seq[0].S));
+    const Plan pl = c.cap_splits
+                        ? make_plan(c.num_sms, cs.B, cs.seq[0].T, max_vis, c.partial_words, c.n_counters)
+                        : make_plan(c.num_sms, cs.B, cs.seq[0].T, max_vis);
+    if (plan_partial_words(pl, cs.B, cs.seq[0].T) > c.partial_words ||
+        plan_counters(pl, cs.B) > c.n_counters)
+      return c.cap_splits ? DS4IDX_ERR_SCRATCH_LIMIT : DS4IDX_ERR_INVALID_ARG;
+    for (int b = 0; b < cs.B; ++b) {
+      n_qb[b] = pl.n_qb;
+      n_splits[b] = pl.n_splits;
+    }
+    tps = pl.tiles_per_split;
+  } else {
+    plan_varlen(c.num_sms, cs, nq, c.partial_words, c.n_counters, n_qb, n_splits, &tps);
   }
-  if (plan_partial_words(pl, B, T) > c.partial_words || plan_counters(pl, B) > c.n_counters)
-    return c.cap_splits ? DS4IDX_ERR_SCRATCH_LIMIT : DS4IDX_ERR_INVALID_ARG;
-
-  if (!encode_rows(&call->tq, q, c.dtype, T * kHeads, B, kHeads * pl.nq))
-    return DS4IDX_ERR_INVALID_ARG;
-  if (!encode_rows(&call->tk, kcache, c.dtype, S, B, kTileKeys)) return DS4IDX_ERR_INVALID_ARG;
 
   KParams& kp = call->kp;
   std::memset(&kp, 0, sizeof kp);
-  kp.w = w;
-  kp.kscale = kscale;
-  kp.out_idx = out_idx;
-  kp.out_score = out_score;
+  int64_t list = 0, tickets = 0, ctas = 0;
+  const size_t per_split = nq == 1 ? static_cast<size_t>(kSlotWords) : static_cast<size_t>(kTopK);
+  for (int b = 0; b < cs.B; ++b) {
+    SeqDesc& d = kp.seq[b];
+    const SeqSpec& q = cs.seq[b];
+    d.T = q.T;
+    d.S = q.S;
+    d.pos = q.pos;
+    d.q_row0 = q.q_row0;
+    d.k_row0 = q.k_row0;
+    d.n_qb = n_qb[b];
+    d.n_splits = n_splits[b];
+    d.tiles_per_split = tps;
+    d.list0 = list;
+    d.ticket0 = static_cast<int32_t>(tickets);
+    d.cta0 = static_cast<int32_t>(ctas);
+    d.pt_row = b;
+    if (n_splits[b] > 1) {
+      list += static_cast<int64_t>(q.T) * n_splits[b] * static_cast<int64_t>(per_split);
+      tickets += n_qb[b];
+    }
+    ctas += static_cast<int64_t>(n_qb[b]) * n_splits[b];
+  }
+  if (static_cast<size_t>(list) > c.partial_words || static_cast<size_t>(tickets) > c.n_counters)
+    return c.cap_splits ? DS4IDX_ERR_SCRATCH_LIMIT : DS4IDX_ERR_INVALID_ARG;
+  if (ctas > 0x7FFFFFFF) return DS4IDX_ERR_INVALID_ARG;
+
+  if (!encode_rows(&call->tq, cs.q, c.dtype, cs.q_rows * kHeads, 1, kHeads * nq))
+    return DS4IDX_ERR_INVALID_ARG;
+  if (!encode_rows(&call->tk, cs.kcache, c.dtype, cs.pool_rows, 1, cs.page_table ? 64 : kTileKeys))
+    return DS4IDX_ERR_INVALID_ARG;
+  kp.w = cs.w;
+  kp.kscale = cs.kscale;
+  kp.out_idx = cs.out_idx;
+  kp.out_score = cs.out_score;
   kp.partial = c.partial;
   kp.counters = c.counters;
-  kp.dense = dense;
+  kp.dense = cs.dense;
   kp.err = c.err;
+  kp.page_table = cs.page_table;
+  kp.pool_rows = cs.pool_rows;
   kp.wait_ns = c.wait_ns;
   kp.withhold = c.withhold;
-  kp.T = T;
-  kp.S = S;
-  kp.B = B;
-  kp.n_qb = pl.n_qb;
-  kp.n_splits = pl.n_splits;
-  kp.tiles_per_split = pl.tiles_per_split;
-  for (int b = 0; b < B; ++b) kp.pos[b] = pos_offsets[b];
-  call->pl = pl;
+  kp.B = cs.B;
+  kp.uniform = cs.uniform ? 1 : 0;
+  kp.page_size = cs.page_size;
+  kp.pt_stride = cs.pt_stride;
+  call->nq = nq;
+  call->grid = ctas;
+  if (ctas == 0) call->noop = true;
+  return DS4IDX_OK;
+}
+
+// The spec of a uniform call: B sequences of T queries and S keys, stored densely one after
+// another (q [B, T, 64, 128], kcache [B, S, 128]).
+int uniform_spec(int32_t B, const void* q, const float* w, const void* kcache,
+                 const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets,
+                 int32_t topk, int32_t* out_idx, float* out_score, float* dense, CallSpec* cs) {
+  if (B < 1 || B > kMaxBatch || !pos_offsets || T < 0 || S < 1) return DS4IDX_ERR_INVALID_ARG;
+  cs->B = B;
+  cs->uniform = true;
+  for (int b = 0; b < B; ++b) {
+    cs->seq[b].T = T;
+    cs->seq[b].S = S;
+    cs->seq[b].pos = pos_offsets[b];
+    cs->seq[b].q_row0 = b * T;
+    cs->seq[b].k_row0 = b * S;
+  }
+  cs->q_rows = B * T;
+  cs->pool_rows = B * S;
+  cs->q = q;
+  cs->w = w;
+  cs->kcache = kcache;
+  cs->kscale = kscale;
+  cs->topk = topk;
+  cs->out_idx = out_idx;
+  cs->out_score = out_score;
+  cs->dense = dense;
   return DS4IDX_OK;
 }
 
 int enqueue(const Ctx& c, const Call& call, void* stream_ptr) {
   if (call.noop) return DS4IDX_OK;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
-  const Plan& pl = call.pl;
   cudaError_t e =
       c.dtype == DS4IDX_BF16
-          ? launch_dt<kDtBf16>(pl.nq, call.dense, call.tq, call.tk, call.kp, pl.grid, stream)
-          : launch_dt<kDtFp8>(pl.nq, call.dense, call.tq, call.tk, call.kp, pl.grid, stream);
+          ? launch_dt<kDtBf16>(call.nq, call.dense, call.tq, call.tk, call.kp, call.grid, stream)
+          : launch_dt<kDtFp8>(call.nq, call.dense, call.tq, call.tk, call.kp, call.grid, stream);
   return e == cudaSuccess ? DS4IDX_OK : DS4IDX_ERR_LAUNCH;
 }
 
-// Shared implementation of the handle-based compute entry points.
+// Shared implementation of the handle-based uniform compute entry points.
 int run(ds4idx_t h, int32_t B, const void* q, const float* w, const void* kcache,
         const float* kscale, int64_t T, int64_t S, const int64_t* pos_offsets, int32_t topk,
         int32_t* out_idx, float* out_score, float* dense, void* stream_ptr) {
   if (!h) return DS4IDX_ERR_INVALID_ARG;
   const Ctx c = handle_ctx(h);
+  CallSpec cs;
+  int st = uniform_spec(B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
+                        dense, &cs);
+  if (st != DS4IDX_OK) return st;
   Call call;
-  const int st = prepare(c, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
-                         dense, &call);
+  st = prepare(c, cs, &call);
   if (st != DS4IDX_OK) return st;
   return enqueue(c, call, stream_ptr);
 }
@@ -441,6 +608,47 @@ int ds4idx_score_topk_batched(ds4idx_t h, int32_t B, const void* q, const float*
                               float* out_score, void* stream) {
   return run(h, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score, nullptr,
              stream);
+}
+
+int ds4idx_score_topk_varlen(ds4idx_t h, int32_t B, const void* q, const float* w,
+                             const int64_t* cu_seqlens_q, const void* kcache, const float* kscale,
+                             int64_t pool_rows, const int64_t* kv_start,
+                             const int32_t* page_table, int32_t page_size, int32_t pages_per_seq,
+                             const int64_t* seq_lens, const int64_t* pos_offsets, int32_t topk,
+                             int32_t* out_idx, float* out_score, void* stream) {
+  if (!h || B < 1 || B > kMaxBatch || !cu_seqlens_q || !seq_lens || !pos_offsets)
+    return DS4IDX_ERR_INVALID_ARG;
+  if ((kv_start == nullptr) == (page_table == nullptr)) return DS4IDX_ERR_INVALID_ARG;
+  if (cu_seqlens_q[0] != 0) return DS4IDX_ERR_INVALID_ARG;
+  CallSpec cs;
+  cs.B = B;
+  cs.uniform = false;
+  for (int b = 0; b < B; ++b) {
+    if (cu_seqlens_q[b + 1] < cu_seqlens_q[b]) return DS4IDX_ERR_INVALID_ARG;
+    cs.seq[b].T = cu_seqlens_q[b + 1] - cu_seqlens_q[b];
+    cs.seq[b].S = seq_lens[b];
+    cs.seq[b].pos = pos_offsets[b];
+    cs.seq[b].q_row0 = cu_seqlens_q[b];
+    cs.seq[b].k_row0 = kv_start ? kv_start[b] : 0;
+  }
+  cs.q_rows = cu_seqlens_q[B];
+  cs.pool_rows = pool_rows;
+  cs.q = q;
+  cs.w = w;
+  cs.kcache = kcache;
+  cs.kscale = kscale;
+  cs.page_table = page_table;
+  cs.page_size = page_size;
+  cs.pt_stride = pages_per_seq;
+  cs.topk = topk;
+  cs.out_idx = out_idx;
+  cs.out_score = out_score;
+  Ctx c = handle_ctx(h);
+  c.cap_splits = true;  // split lists of mixed lengths are fitted to the handle's workspace
+  Call call;
+  const int st = prepare(c, cs, &call);
+  if (st != DS4IDX_OK) return st;
+  return enqueue(c, call, stream);
 }
 
 int ds4idx_score_dense_debug(ds4idx_t h, const void* q, const float* w, const void* kcache,
@@ -595,9 +803,12 @@ extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const
   c.counters = reinterpret_cast<uint32_t*>(d.scratch + kNoAllocListWords + 32);
   c.n_counters = kNoAllocTickets;
   c.cap_splits = true;
+  CallSpec cs;
+  int vs = uniform_spec(B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
+                        nullptr, &cs);
+  if (vs != DS4IDX_OK) return vs;
   Call call;
-  const int vs = prepare(c, B, q, w, kcache, kscale, T, S, pos_offsets, topk, out_idx, out_score,
-                         nullptr, &call);
+  vs = prepare(c, cs, &call);
   if (vs != DS4IDX_OK) return vs;
   // Valid call: the array keeps the previous call's contents, so clear the error word and the
   // tickets on the stream right before the launch.

@@ -85,22 +85,53 @@ struct RankArea {
         hdr(rhist + 256) {}
 };
 
+// One sequence of a call: its queries, its keys, its position and its share of the grid.
+struct SeqDesc {
+  int64_t T;          // queries
+  int64_t S;          // keys in its cache
+  int64_t pos;        // position of query 0 (query t sits at pos + t)
+  int64_t q_row0;     // row of query 0 in the packed q [*, 64, 128], w, out_idx and out_score
+  int64_t k_row0;     // row of key 0 in the key pool (contiguous caches)
+  int64_t list0;      // first word of its split lists in `partial`
+  int32_t n_qb;       // query blocks of NQ queries
+  int32_t n_splits;   // key splits per query block
+  int32_t tiles_per_split;
+  int32_t cta0;       // first CTA of its work (calls that are not uniform)
+  int32_t ticket0;    // first of its split tickets in `counters`
+  int32_t pt_row;     // its row of the page table (paged caches)
+};
+
 struct KParams {
-  const float* w;        // [B, T, 64]
-  const float* kscale;   // [B, S] (FP8) or null
-  int32_t* out_idx;      // [B, T, 512]
-  float* out_score;      // [B, T, 512] or null
-  uint64_t* partial;     // per-split lists when n_splits > 1: [B, T, n_splits, 512] words, or
-                         // [B, n_splits, kSlotWords] slots for one-query CTAs
-  uint32_t* counters;    // [B * n_qb] split tickets (zero between calls) when n_splits > 1
-  float* dense;          // [T, S] scores (debug variant)
+  const float* w;        // [rows, 64]
+  const float* kscale;   // [pool rows] (FP8) or null
+  int32_t* out_idx;      // [rows, 512]
+  float* out_score;      // [rows, 512] or null
+  uint64_t* partial;     // per-split lists of split plans: per query 512 words per split, or one
+                         // slot of kSlotWords per split for one-query CTAs
+  uint32_t* counters;    // split tickets (zero between calls)
+  float* dense;          // [T, S] scores (debug variant, one sequence)
   uint32_t* err;         // device error word
+  const int32_t* page_table;  // [*, pt_stride] page ids (paged key pool), or null (contiguous)
+  int64_t pool_rows;     // rows of the key pool
   uint64_t wait_ns;      // limit of one bounded mbarrier wait (kWaitLimitNs)
   int32_t withhold;      // test only: CTA 0's first selector withholds its first ring release
-  int64_t T, S;
-  int32_t B, n_qb, n_splits, tiles_per_split;
-  int64_t pos[kMaxBatch];
+  int32_t B;
+  int32_t uniform;       // every sequence has the same plan: CTA i serves sequence i % B
+  int32_t page_size;     // keys per page (a multiple of 64) when paged
+  int32_t pt_stride;     // page-table entries per sequence
+  SeqDesc seq[kMaxBatch];
 };
+
+// Pool row of key `key` (< sd.S) of a sequence. A page id outside the pool (the caller's
+// mistake) gives pool_rows, a row past the pool: TMA loads it as zeros and the scale reads skip
+// it, so a bad page table yields wrong scores, never an out-of-bounds access.
+__device__ __forceinline__ int64_t key_row(const KParams& p, const SeqDesc& sd, int64_t key) {
+  if (p.page_table == nullptr) return sd.k_row0 + key;
+  const int64_t page = __ldg(p.page_table + static_cast<int64_t>(sd.pt_row) * p.pt_stride +
+                             key / p.page_size);
+  const int64_t row = page * p.page_size + key % p.page_size;
+  return (page >= 0 && row < p.pool_rows) ? row : p.pool_rows;
+}
 
 template <int DT, int NQ, bool DENSE>
 struct KCfg {
@@ -264,14 +295,14 @@ __device__ void publish_slot(uint64_t* slot, const uint64_t* words, int cnt, uin
 // words), the 512 best words are radix-selected with all warps, and then either published
 // unordered as this split's list or sorted once and written as the output row.
 template <class C>
-__device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split,
+__device__ void finish_cta_select(const KParams& p, const SeqDesc& sd, int64_t t0, int split,
                                   uint64_t* pools, const uint32_t* pool_n, uint64_t* stage,
                                   uint32_t* hist, uint32_t* scratch, int warp, int lane) {
   constexpr int R = kTopK / 32;
   constexpr int kWords = C::kSelPerQuery * C::kPool;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
-    if (t >= p.T) break;
+    if (t >= sd.T) break;
     uint64_t* base = pools + q * kWords;
     for (int sw = 0; sw < C::kSelPerQuery; ++sw) {
       const int used = static_cast<int>(pool_n[q * C::kSelPerQuery + sw]);
@@ -279,13 +310,13 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
     }
     __syncthreads();
     const int cnt = cta_select<kTopK, C::kThreads>(base, kWords, stage, hist, scratch);
-    const int64_t row = static_cast<int64_t>(b) * p.T + t;
-    if (p.n_splits > 1) {
+    const int64_t row = sd.q_row0 + t;
+    if (sd.n_splits > 1) {
       if constexpr (C::kHistSel) {
-        publish_slot<C::kThreads>(p.partial + (row * p.n_splits + split) * kSlotWords, stage, cnt,
-                                  hist, scratch, warp, lane);
+        publish_slot<C::kThreads>(p.partial + sd.list0 + (t * sd.n_splits + split) * kSlotWords,
+                                  stage, cnt, hist, scratch, warp, lane);
       } else {
-        uint64_t* dst = p.partial + (row * p.n_splits + split) * kTopK;
+        uint64_t* dst = p.partial + sd.list0 + (t * sd.n_splits + split) * kTopK;
         for (int i = threadIdx.x; i < kTopK; i += C::kThreads) dst[i] = i < cnt ? stage[i] : 0ull;
       }
     } else if (warp == 0) {
@@ -299,7 +330,7 @@ __device__ void finish_cta_select(const KParams& p, int b, int64_t t0, int split
   }
   // Lists are made visible GPU-wide by the ticket's fence (thread 0, after a CTA barrier);
   // this orders the generic-proxy writes before the bulk copies that will read them.
-  if (p.n_splits > 1) fence_proxy_async_global();
+  if (sd.n_splits > 1) fence_proxy_async_global();
 }
 
 // Writes the (up to) 512 best of the distinct words in ra.sv[0..n) whose bins lie in [lo, hi]
@@ -403,7 +434,7 @@ struct ScoreWords {
 // otherwise they are ranked and written. A full candidate list, or too many keys at b* (exact
 // ties, a very flat score distribution), fall back to a radix select over all buffered scores.
 template <class C>
-__device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint32_t* bins,
+__device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int split, uint32_t* bins,
                             const uint16_t* cand, const uint32_t* ncand, const float* sbuf,
                             int n_tiles, int64_t key0, int64_t vis_end, uint32_t floor_bin,
                             uint32_t maxbin, uint64_t* stage, uint32_t* scratch, int warp,
@@ -411,7 +442,7 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
   constexpr int NT = C::kThreads;
   constexpr int kWarps = NT / 32;
   constexpr int kSegs = C::kEpiWarps;
-  const int64_t row = static_cast<int64_t>(b) * p.T + t0;
+  const int64_t row = sd.q_row0 + t0;
   if (warp == 0) {
     uint32_t m;
     const uint32_t bs =
@@ -427,8 +458,9 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
   bool listed = true;
 #pragma unroll
   for (int s = 0; s < kSegs; ++s) listed = listed && ncand[s] <= static_cast<uint32_t>(C::kCandSeg);
-  const bool split_plan = p.n_splits > 1;
-  uint64_t* slot = split_plan ? p.partial + (row * p.n_splits + split) * kSlotWords : nullptr;
+  const bool split_plan = sd.n_splits > 1;
+  uint64_t* slot =
+      split_plan ? p.partial + sd.list0 + (t0 * sd.n_splits + split) * kSlotWords : nullptr;
   RankArea ra(reinterpret_cast<uint8_t*>(stage));
   const bool fast = listed && (split_plan ? m <= kSlotListCap
                                           : (m <= kSurvCap && maxbin - bstar < kRankBins));
@@ -525,7 +557,7 @@ __device__ void finish_hist(const KParams& p, int b, int64_t t0, int split, uint
 // words with bin >= G. More of them than the ranking takes fall back to a radix select over all
 // lists and one CTA-wide sort.
 template <class C>
-__device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* buf,
+__device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0, uint64_t* buf,
                                  uint8_t* area, uint64_t* gbar, volatile uint32_t* abort_flag,
                                  uint32_t* scratch, int warp, int lane) {
   constexpr int NT = C::kThreads;
@@ -540,9 +572,9 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
   uint32_t* hnb = hlo + 64;   // [64] window widths
   uint32_t* hn = hnb + 64;    // [64] words to take from each list
   uint32_t* hpre = hn + 64;   // [65] their offsets in sv (rounded up to even)
-  const int ns = p.n_splits;
-  const int64_t row = static_cast<int64_t>(b) * p.T + t0;
-  const uint64_t* slots = p.partial + row * ns * kSlotWords;
+  const int ns = sd.n_splits;
+  const int64_t row = sd.q_row0 + t0;
+  const uint64_t* slots = p.partial + sd.list0 + t0 * ns * kSlotWords;
   for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
   fence_proxy_async_smem();  // earlier generic accesses to the copy targets precede the copies
   __syncthreads();
@@ -687,7 +719,7 @@ __device__ void merge_hist_slots(const KParams& p, int b, int64_t t0, uint64_t* 
 // them once in registers and write the output row. Lists that do not fit at once are folded in
 // rounds (the 512 survivors of a round stay at the front of the gather area).
 template <class C>
-__device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t* stage,
+__device__ void merge_split_lists(const KParams& p, const SeqDesc& sd, int64_t t0, uint64_t* stage,
                                   uint32_t* hist, uint32_t* scratch, int warp, int lane) {
   constexpr int kStageWords = C::kStages * C::kKBytes / 8;
   constexpr int kCap = kStageWords - kTopK;  // gather area; the last 512 words receive selects
@@ -695,12 +727,12 @@ __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t*
   uint64_t* sel = stage + kCap;
   for (int q = 0; q < C::kN / kHeads; ++q) {
     const int64_t t = t0 + q;
-    if (t >= p.T) break;
-    const int64_t row = static_cast<int64_t>(b) * p.T + t;
-    const uint64_t* lists = p.partial + row * p.n_splits * kTopK;
+    if (t >= sd.T) break;
+    const int64_t row = sd.q_row0 + t;
+    const uint64_t* lists = p.partial + sd.list0 + t * sd.n_splits * kTopK;
     int n = 0;  // words already in the gather area (survivors of earlier rounds)
-    for (int sp0 = 0; sp0 < p.n_splits; sp0 += kListsPerRound) {
-      const int nl = p.n_splits - sp0 < kListsPerRound ? p.n_splits - sp0 : kListsPerRound;
+    for (int sp0 = 0; sp0 < sd.n_splits; sp0 += kListsPerRound) {
+      const int nl = sd.n_splits - sp0 < kListsPerRound ? sd.n_splits - sp0 : kListsPerRound;
       const uint4* src = reinterpret_cast<const uint4*>(lists + static_cast<int64_t>(sp0) * kTopK);
       uint4* dst = reinterpret_cast<uint4*>(stage + n);
       const int n4 = nl * kTopK / 2;
@@ -708,7 +740,7 @@ __device__ void merge_split_lists(const KParams& p, int b, int64_t t0, uint64_t*
       for (int i = threadIdx.x; i < n4; i += C::kThreads) dst[i] = src[i];
       __syncthreads();
       n += nl * kTopK;
-      if (sp0 + nl < p.n_splits) {  // another round follows: keep only the 512 best
+      if (sp0 + nl < sd.n_splits) {  // another round follows: keep only the 512 best
         const int kept = cta_select<kTopK, C::kThreads>(stage, n, sel, hist, scratch);
         // zero-padded to exactly 512 words, so the next round's copy stays 16-byte aligned
         for (int i = threadIdx.x; i < kTopK; i += C::kThreads) stage[i] = i < kept ? sel[i] : 0ull;
@@ -779,32 +811,43 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work item: longest query blocks first; batches and key splits innermost
+  // ---- work item: longest query blocks first, key splits innermost. Uniform calls interleave
+  // the sequences (CTA i serves sequence i % B); otherwise each sequence owns a CTA range.
   const int wid = blockIdx.x;
-  const int b = wid % p.B;
-  const int rest = wid / p.B;
-  const int split = rest % p.n_splits;
-  const int qb = p.n_qb - 1 - rest / p.n_splits;
+  int b, rest;
+  if (p.uniform) {
+    b = wid % p.B;
+    rest = wid / p.B;
+  } else {
+    b = 0;
+    while (b + 1 < p.B && p.seq[b + 1].cta0 <= wid) ++b;
+    rest = wid - p.seq[b].cta0;
+  }
+  const SeqDesc sd = p.seq[b];  // this sequence's fields, in registers
+  const bool paged = p.page_table != nullptr;
+  const int split = rest % sd.n_splits;
+  const int qb = sd.n_qb - 1 - rest / sd.n_splits;
   const int64_t t0 = static_cast<int64_t>(qb) * NQ;
-  const int64_t t_last = (t0 + NQ < p.T ? t0 + NQ : p.T) - 1;
-  const int64_t pos_b = p.pos[b];
+  const int64_t t_last = (t0 + NQ < sd.T ? t0 + NQ : sd.T) - 1;
+  const int64_t pos_b = sd.pos;
+  const int64_t S_b = sd.S;
   int tile_lo, n_tiles;
   if (DENSE) {
     tile_lo = 0;
-    n_tiles = static_cast<int>((p.S + kTileKeys - 1) / kTileKeys);
+    n_tiles = static_cast<int>((S_b + kTileKeys - 1) / kTileKeys);
   } else {
     const int64_t p_last = pos_b + t_last;
-    const int64_t vis_end = (p_last < p.S - 1 ? p_last : p.S - 1) + 1;
+    const int64_t vis_end = (p_last < S_b - 1 ? p_last : S_b - 1) + 1;
     const int tiles_total = static_cast<int>((vis_end + kTileKeys - 1) / kTileKeys);
-    tile_lo = split * p.tiles_per_split;
-    const int hi = tile_lo + p.tiles_per_split < tiles_total ? tile_lo + p.tiles_per_split
-                                                              : tiles_total;
+    tile_lo = split * sd.tiles_per_split;
+    const int hi = tile_lo + sd.tiles_per_split < tiles_total ? tile_lo + sd.tiles_per_split
+                                                               : tiles_total;
     n_tiles = hi > tile_lo ? hi - tile_lo : 0;
   }
 
   const bool buffered = C::kBufTiles > 0 && n_tiles <= C::kBufTiles;
   // Keys a one-query CTA's query can see: [0, vis_q).
-  const int64_t vis_q = (pos_b + t0 < p.S - 1 ? pos_b + t0 : p.S - 1) + 1;
+  const int64_t vis_q = (pos_b + t0 < S_b - 1 ? pos_b + t0 : S_b - 1) + 1;
 
   // ---- setup
   if (threadIdx.x == 0) {
@@ -844,7 +887,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   griddep_wait();
   for (int i = threadIdx.x; i < NQ * kHeads; i += C::kThreads) {
     const int64_t t = t0 + i / kHeads;
-    sW[i] = t < p.T ? p.w[(static_cast<int64_t>(b) * p.T + t) * kHeads + (i % kHeads)] : 0.f;
+    sW[i] = t < sd.T ? p.w[(sd.q_row0 + t) * kHeads + (i % kHeads)] : 0.f;
   }
   tc_fence_before();
   __syncthreads();
@@ -857,7 +900,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       mbar_arrive_expect_tx(qfull, C::kQBytes);
       for (int h = 0; h < C::kHalves; ++h)
         tma_load_3d(sQ + h * (C::kN * 128), &tmap_q, qfull, h * 64 * (DT == kDtBf16 ? 1 : 2),
-                    static_cast<int32_t>(t0 * kHeads), b);
+                    static_cast<int32_t>((sd.q_row0 + t0) * kHeads), 0);
       int it = 0;
       for (; it < n_tiles; ++it) {
         const int st = it % C::kStages;
@@ -865,10 +908,24 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         if (!mbar_wait<C::kWaitHint>(&empty[st], ph ^ 1u, s_abort, p.err, p.wait_ns)) break;
         mbar_arrive_expect_tx(&full[st], C::kKBytes);
         uint8_t* dst = sK + st * C::kKBytes;
-        const int32_t key0 = (tile_lo + it) * kTileKeys;
-        for (int h = 0; h < C::kHalves; ++h)
-          tma_load_3d(dst + h * (kTileKeys * 128), &tmap_k, &full[st],
-                      h * 64 * (DT == kDtBf16 ? 1 : 2), key0, b);
+        const int64_t key0 = static_cast<int64_t>(tile_lo + it) * kTileKeys;
+        if (!paged) {
+          // contiguous pool: one 128-row box per swizzle column (rows past the pool read 0)
+          const int32_t row = static_cast<int32_t>(sd.k_row0 + key0);
+          for (int h = 0; h < C::kHalves; ++h)
+            tma_load_3d(dst + h * (kTileKeys * 128), &tmap_k, &full[st],
+                        h * 64 * (DT == kDtBf16 ? 1 : 2), row, 0);
+        } else {
+          // paged pool: two 64-row boxes (a page holds a multiple of 64 keys); a box past the
+          // sequence's keys reads rows past the pool, which load as zeros
+          for (int sub = 0; sub < 2; ++sub) {
+            const int64_t key = key0 + sub * 64;
+            const int32_t row = static_cast<int32_t>(key < S_b ? key_row(p, sd, key) : p.pool_rows);
+            for (int h = 0; h < C::kHalves; ++h)
+              tma_load_3d(dst + h * (kTileKeys * 128) + sub * (64 * 128), &tmap_k, &full[st],
+                          h * 64 * (DT == kDtBf16 ? 1 : 2), row, 0);
+          }
+        }
       }
       // Never leave the CTA with copies in flight: wait for the last load of each stage and
       // for the Q block, also after an abort (the waits ignore the abort flag; the copies
@@ -927,10 +984,13 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     // FP8 key scales are read two tiles ahead so their global-memory latency stays hidden
     // (decode streams the cache once, so these reads miss in L2).
-    const float* kscale_b = DT == kDtFp8 ? p.kscale + static_cast<int64_t>(b) * p.S : nullptr;
+    const float* kscale_c = DT == kDtFp8 && !paged ? p.kscale + sd.k_row0 : nullptr;
     auto load_scale = [&](int tile) -> float {
       const int64_t k = static_cast<int64_t>(tile_lo + tile) * kTileKeys + quad * 32 + lane;
-      return (tile < n_tiles && k < p.S) ? __ldg(kscale_b + k) : 0.f;
+      if (tile >= n_tiles || k >= S_b) return 0.f;
+      if (!paged) return __ldg(kscale_c + k);
+      const int64_t row = key_row(p, sd, k);
+      return row < p.pool_rows ? __ldg(p.kscale + row) : 0.f;
     };
     float ks_next0 = 1.f, ks_next1 = 1.f;
     uint32_t own_cand = 0u;                                  // buffered mode: keys listed
@@ -992,9 +1052,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
           if (DT == kDtFp8) score *= ks;
           if (DENSE) {
             const int64_t t = t0 + q;
-            if (t < p.T && key < p.S) {
+            if (t < sd.T && key < S_b) {
               const bool vis = key <= pos_b + t;
-              p.dense[t * p.S + key] = vis ? score : -__int_as_float(0x7f800000);
+              p.dense[t * S_b + key] = vis ? score : -__int_as_float(0x7f800000);
             }
           } else if (buffered) {
             // Running cut: a key is a candidate when its bin reaches the cut bin, which some
@@ -1058,9 +1118,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     uint64_t* pool = sPool + sidx * C::kPool;
     uint32_t* hist = sHist + sidx * 256;
     const int64_t t = t0 + q;
-    const bool valid = t < p.T;
+    const bool valid = t < sd.T;
     const int64_t pt = pos_b + t;
-    const int64_t vis_end = valid ? (pt < p.S - 1 ? pt : p.S - 1) + 1 : 0;
+    const int64_t vis_end = valid ? (pt < S_b - 1 ? pt : S_b - 1) + 1 : 0;
     const uint32_t lt_mask = (1u << lane) - 1u;
     uint64_t theta = 0ull;  // exact 512th best word this warp has seen (0 until 512 were seen)
     int n = 0;              // words in the pool
@@ -1097,7 +1157,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         if (lane == 0) s_theta[sidx] = theta;
       }
     }
-    if (C::kSelPerQuery > 1 || p.n_splits > 1) {
+    if (C::kSelPerQuery > 1 || sd.n_splits > 1) {
       // Finished with a CTA-wide select after the role loops (every warp helps).
       if (lane == 0) s_pool_n[sidx] = static_cast<uint32_t>(n);
     } else {
@@ -1112,7 +1172,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         v[r] = i < n ? pool[i] : 0ull;
       }
       warp_sort_desc<R>(v, lane);
-      if (valid && !*s_abort) write_output<R>(p, static_cast<int64_t>(b) * p.T + t, v, lane);
+      if (valid && !*s_abort) write_output<R>(p, sd.q_row0 + t, v, lane);
     }
   }
 
@@ -1126,32 +1186,32 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   }
   if (!DENSE && !*s_abort) {
     if (buffered)
-      finish_hist<C>(p, b, t0, split, s_bins, s_cand, s_ncand, sBuf, n_tiles,
+      finish_hist<C>(p, sd, t0, split, s_bins, s_cand, s_ncand, sBuf, n_tiles,
                      static_cast<int64_t>(tile_lo) * kTileKeys, vis_q, *s_cut, *s_maxbin,
                      reinterpret_cast<uint64_t*>(sK), s_scratch, warp, lane);
-    else if (C::kSelPerQuery > 1 || p.n_splits > 1)
-      finish_cta_select<C>(p, b, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK),
+    else if (C::kSelPerQuery > 1 || sd.n_splits > 1)
+      finish_cta_select<C>(p, sd, t0, split, sPool, s_pool_n, reinterpret_cast<uint64_t*>(sK),
                            sHist, s_scratch, warp, lane);
   }
-  if (!DENSE && p.n_splits > 1) {
+  if (!DENSE && sd.n_splits > 1) {
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
-    uint32_t* ticket = p.counters + static_cast<int64_t>(b) * p.n_qb + qb;
+    uint32_t* ticket = p.counters + sd.ticket0 + qb;
     __syncthreads();  // every thread's list writes (and proxy fence) precede the ticket
     if (threadIdx.x == 0) {
       __threadfence();
-      *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(p.n_splits - 1) ? 1u : 0u;
+      *s_last = atomicAdd(ticket, 1u) == static_cast<uint32_t>(sd.n_splits - 1) ? 1u : 0u;
     }
     __syncthreads();
     if (*s_last) {
       __threadfence();
       if (!*s_abort) {
         if constexpr (C::kHistSel)
-          merge_hist_slots<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), smem + C::kOffHist, gbar,
-                              s_abort, s_scratch, warp, lane);
+          merge_hist_slots<C>(p, sd, t0, reinterpret_cast<uint64_t*>(sK), smem + C::kOffHist,
+                              gbar, s_abort, s_scratch, warp, lane);
         else
-          merge_split_lists<C>(p, b, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch, warp,
-                               lane);
+          merge_split_lists<C>(p, sd, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch,
+                               warp, lane);
       }
       if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
     }

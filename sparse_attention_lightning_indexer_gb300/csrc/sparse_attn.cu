@@ -1,0 +1,397 @@
+// Sparse attention over the indexer's selected keys, for sm_103a: the step that consumes the
+// Top-512 lists ("DeepSeek V4 Flash 추론을 1.6초로 줄인 ds4 최적화", 용어 해설: sparse attention
+// computes only some token pairs, and the Lightning Indexer chooses them).
+//
+// For query token t and head h over its selected positions J(t) (the indexer's out_idx row,
+// -1 = empty), with one latent row kv[s] (d_qk = 576) per position shared by all 128 heads:
+//     s_j = scale * q[t,h,:] . kv[j,:],   o[t,h,:] = sum_j softmax(s)_j kv[j, 0:512],
+//     lse[t,h] = log sum_j exp(s_j).
+//
+// One CTA per token, all 128 heads (heads = TMEM lanes, so each softmax row lives in one
+// thread). Warps 0-3 are the softmax / output warps (thread h owns head h), warp 4 gathers rows
+// with TMA (tile::gather4 of 4 rows x 64 dims per instruction), warp 5 issues tcgen05.mma.
+//   A  S[128 heads x 512 keys] = Q K^T accumulates over 9 chunks of 64 dims: per chunk a Q
+//      chunk (tiled TMA) and the chunk of all 512 gathered key rows; 4 MMAs of N = 128 keys per
+//      16-dim step into TMEM columns 0..511.
+//   B  two passes over S in TMEM: the row maximum, then p = exp2(s * scale * log2 e - max),
+//      summed in fp32 and stored as bf16 into shared memory in the K-major 128-byte-swizzled
+//      layout of an MMA A operand (8 blocks of 64 keys).
+//   C  O[128 x 512] = P V in two halves of 256 value dims (TMEM columns 256..511, free once S is
+//      read): V chunks of 64 keys x 256 dims are gathered again and fed as an MN-major B operand.
+//      The output warps scale each half by 1 / sum and store it as bf16.
+// Shared memory: phase A's two 80 KB stages and phase C's P (128 KB) + two 32 KB V stages share
+// one 192 KB region (the phases of a token never overlap).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ds4idx.h"
+#include "ptx.cuh"
+
+namespace ds4w {
+extern std::atomic<uint64_t>* launch_counter();
+}
+
+namespace ds4a {
+
+using namespace ds4;
+
+constexpr int kH = 128;          // heads = MMA M = TMEM lanes
+constexpr int kDqk = 576;        // key / query width
+constexpr int kDv = 512;         // value width (first kDv dims of a row)
+constexpr int kK = 512;          // selected keys per token
+constexpr int kChunk = 64;       // dims per K chunk (128 bytes of bf16)
+constexpr int kNChunks = kDqk / kChunk;  // 9
+constexpr int kAStageBytes = kH * 128 + kK * 128;  // Q chunk 16 KB + key chunk 64 KB
+constexpr int kVKeys = 64;       // keys per V chunk
+constexpr int kVStageBytes = 4 * kVKeys * 128;     // 4 blocks of 64 dims: 32 KB
+constexpr int kPBytes = (kK / 64) * kH * 128;      // 8 blocks of 64 keys: 128 KB
+constexpr int kOffP = 0;
+constexpr int kOffV = kPBytes;
+constexpr int kRegion = kPBytes + 2 * kVStageBytes;  // 192 KB
+static_assert(2 * kAStageBytes <= kRegion, "phase A stages fit the shared region");
+constexpr int kOffRows = kRegion;                   // int32 gather rows [512]
+constexpr int kOffMask = kOffRows + kK * 4;         // uint32 validity words [16]
+constexpr int kOffBars = kOffMask + 64;
+constexpr int kNumBars = 2 + 2 + 1 + 1 + 2 + 2 + 1 + 1;
+constexpr int kOffMisc = kOffBars + kNumBars * 8;
+constexpr int kSmemBytes = kOffMisc + 32 + 1024;
+constexpr int kThreads = 6 * 32;
+constexpr int kProducer = 4, kMma = 5;
+// B operand of P.V: V chunk rows are keys (the K dimension), 64 value dims per 128-byte row
+// (the N dimension): an MN-major operand. Atoms of 8 keys x 64 dims (1 KB) repeat every 1 KB
+// along K and every kVKeys * 128 bytes along N.
+constexpr uint32_t kVStrideN = kVKeys * 128;
+constexpr uint32_t kVStrideK = 1024;
+
+__device__ uint32_t g_err;  // bounded-wait timeouts, read by ds4idx_sparse_attention_status
+
+struct SAParams {
+  const int32_t* idx;      // [T, 512]
+  const int64_t* row0;     // [T] kv row of key 0 (or null)
+  uint16_t* out;           // [T, 128, 512] bf16
+  float* lse;              // [T, 128] or null
+  int64_t T;
+  int64_t kv_rows;
+  float scale_log2;        // scale * log2(e)
+};
+
+__device__ __forceinline__ void gather4(void* dst, const CUtensorMap* m, uint64_t* bar, int32_t col,
+                                        int32_t r0, int32_t r1, int32_t r2, int32_t r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(col), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
+                                            int32_t x, int32_t y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// Shared-memory descriptor of an MN-major operand in the 128-byte swizzle layout.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t stride_n,
+                                                       uint32_t stride_k) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((stride_n >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>((stride_k >> 4) & 0x3FFFu) << 32;  // stride byte offset
+  d |= static_cast<uint64_t>(1u) << 46;
+  d |= static_cast<uint64_t>(2u) << 61;
+  return d;
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q,
+                       const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ SAParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  int32_t* s_rows = reinterpret_cast<int32_t*>(smem + kOffRows);
+  uint32_t* s_mask = reinterpret_cast<uint32_t*>(smem + kOffMask);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBars);
+  uint64_t* a_full = bars;        // [2]
+  uint64_t* a_empty = bars + 2;   // [2]
+  uint64_t* s_ready = bars + 4;
+  uint64_t* p_ready = bars + 5;
+  uint64_t* v_full = bars + 6;    // [2]
+  uint64_t* v_empty = bars + 8;   // [2]
+  uint64_t* o_ready = bars + 10;
+  uint64_t* o_free = bars + 11;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t t = blockIdx.x;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&a_full[i], 1);
+      mbar_init(&a_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
+    }
+    mbar_init(s_ready, 1);
+    mbar_init(p_ready, 4);
+    mbar_init(o_ready, 1);
+    mbar_init(o_free, 4);
+    *s_abort = 0u;
+    fence_mbar_init();
+  }
+  if (warp == kMma) {
+    tmem_alloc(s_tmem, 512);
+    tmem_relinquish();
+  }
+  // Gather rows (an empty slot gathers row 0; its score is masked) and validity words.
+  const int64_t r0 = p.row0 ? p.row0[t] : 0;
+  for (int j = threadIdx.x; j < kK; j += kThreads) {
+    const int32_t k = p.idx[t * kK + j];
+    const int64_t r = r0 + k;
+    const bool ok = k >= 0 && r >= 0 && r < p.kv_rows;
+    s_rows[j] = ok ? static_cast<int32_t>(r) : 0;
+    const uint32_t m = __ballot_sync(0xffffffffu, ok);
+    if (lane == 0) s_mask[j >> 5] = m;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  uint32_t* err = &g_err;
+
+  if (warp == kProducer) {
+    // ---------------- gathers
+    for (int c = 0; c < kNChunks; ++c) {
+      const int st = c & 1;
+      if (!mbar_wait_warp(&a_empty[st], ((c >> 1) & 1) ^ 1u, s_abort, err)) break;
+      uint8_t* base = smem + st * kAStageBytes;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&a_full[st], kAStageBytes);
+        tma_load_2d(base, &tmap_q, &a_full[st], c * kChunk, static_cast<int32_t>(t * kH));
+      }
+      __syncwarp();
+      for (int g = lane; g < kK / 4; g += 32)
+        gather4(base + kH * 128 + g * 512, &tmap_kv, &a_full[st], c * kChunk, s_rows[4 * g],
+                s_rows[4 * g + 1], s_rows[4 * g + 2], s_rows[4 * g + 3]);
+    }
+    // phase C reuses the region: wait until every phase-A MMA has completed
+    if (mbar_wait_warp(s_ready, 0u, s_abort, err)) {
+      for (int i = 0; i < 2 * (kK / kVKeys); ++i) {
+        const int half = i / (kK / kVKeys), kc = i % (kK / kVKeys), st = i & 1;
+        if (!mbar_wait_warp(&v_empty[st], ((i >> 1) & 1) ^ 1u, s_abort, err)) break;
+        uint8_t* base = smem + kOffV + st * kVStageBytes;
+        if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kVStageBytes);
+        __syncwarp();
+        for (int x = lane; x < 4 * (kVKeys / 4); x += 32) {
+          const int nb = x / (kVKeys / 4), g = x % (kVKeys / 4);
+          const int j = kc * kVKeys + 4 * g;
+          gather4(base + nb * kVStrideN + g * 512, &tmap_kv, &v_full[st], half * 256 + nb * 64,
+                  s_rows[j], s_rows[j + 1], s_rows[j + 2], s_rows[j + 3]);
+        }
+      }
+    }
+    // never exit with gathers in flight
+    for (int st = 0; st < 2; ++st) {
+      mbar_drain(&a_full[st], 0u);
+      mbar_drain(&v_full[st], 1u);
+    }
+  } else if (warp == kMma) {
+    // ---------------- MMA issue (one thread)
+    if (lane == 0) {
+      constexpr uint32_t kIdescS = instr_desc(1u, 1u, 128, 128);            // K-major A and B
+      constexpr uint32_t kIdescO = instr_desc(1u, 1u, 128, 256) | (1u << 16);  // B MN-major
+      bool ok = true;
+      for (int c = 0; ok && c < kNChunks; ++c) {
+        const int st = c & 1;
+        if (!(ok = mbar_wait(&a_full[st], (c >> 1) & 1, s_abort, err))) break;
+        tc_fence_after();
+        const uint32_t qa = smem_u32(smem + st * kAStageBytes);
+        const uint32_t kb = qa + kH * 128;
+        for (int j = 0; j < 4; ++j)
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tmem + 128 * j, smem_desc_sw128(qa + ks * 32),
+                     smem_desc_sw128(kb + j * 128 * 128 + ks * 32), kIdescS, (c | ks) ? 1u : 0u);
+        mma_commit(&a_empty[st]);
+      }
+      mma_commit(s_ready);
+      if (ok) ok = mbar_wait(p_ready, 0u, s_abort, err);
+      tc_fence_after();
+      const uint32_t pa = smem_u32(smem + kOffP);
+      for (int i = 0; ok && i < 2 * (kK / kVKeys); ++i) {
+        const int half = i / (kK / kVKeys), kc = i % (kK / kVKeys), st = i & 1;
+        if (half == 1 && kc == 0) {
+          if (!(ok = mbar_wait(o_free, 0u, s_abort, err))) break;
+          tc_fence_after();
+        }
+        if (!(ok = mbar_wait(&v_full[st], (i >> 1) & 1, s_abort, err))) break;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + kOffV + st * kVStageBytes);
+        for (int ks = 0; ks < kVKeys / 16; ++ks)
+          mma_bf16(tmem + 256, smem_desc_sw128(pa + kc * (kH * 128) + ks * 32),
+                   smem_desc_mn_sw128(vb + ks * 16 * 128, kVStrideN, kVStrideK), kIdescO,
+                   (kc | ks) ? 1u : 0u);
+        mma_commit(&v_empty[st]);
+        if (kc == kK / kVKeys - 1) mma_commit(o_ready);
+      }
+      // every MMA has completed before TMEM is released (bounded, also after an abort)
+      mbar_drain(s_ready, 0u);
+      mbar_drain(o_ready, 1u);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax and output (thread = head)
+    const int h = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    float m = -__int_as_float(0x7f800000), l = 0.f;
+    bool ok = mbar_wait_warp(s_ready, 0u, s_abort, err);
+    tc_fence_after();
+    if (ok) {
+      uint32_t r[32];
+      for (int i = 0; i < kK / 32; ++i) {
+        tmem_ld32(tmem + lane_base + 32 * i, r);
+        tmem_wait_ld();
+        const uint32_t vm = s_mask[i];
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]) * p.scale_log2);
+      }
+      const float mm = m == -__int_as_float(0x7f800000) ? 0.f : m;
+      for (int i = 0; i < kK / 32; ++i) {
+        tmem_ld32(tmem + lane_base + 32 * i, r);
+        tmem_wait_ld();
+        const uint32_t vm = s_mask[i];
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const float p0 = ((vm >> j) & 1u) ? exp2f(__uint_as_float(r[j]) * p.scale_log2 - mm) : 0.f;
+          const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(__uint_as_float(r[j + 1]) * p.scale_log2 - mm) : 0.f;
+          l += p0 + p1;
+          pk[j / 2] = pack_bf16x2(p0, p1);
+        }
+        // keys 32i..32i+31 of head h: block i/2, 16-byte chunks (i%2)*4 .. +3 of row h
+        uint8_t* row = smem + kOffP + (i >> 1) * (kH * 128) + h * 128;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int cc = (i & 1) * 4 + u;
+          *reinterpret_cast<uint4*>(row + ((cc ^ (h & 7)) * 16)) =
+              make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        }
+      }
+    }
+    fence_proxy_async_smem();  // P (generic writes) before the MMAs that read it
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(p_ready);
+    if (p.lse)
+      p.lse[t * kH + h] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    uint16_t* orow = p.out + (t * kH + h) * kDv;
+    for (int half = 0; ok && half < 2; ++half) {
+      if (!(ok = mbar_wait_warp(o_ready, static_cast<uint32_t>(half), s_abort, err))) break;
+      tc_fence_after();
+      uint32_t r[32];
+      for (int i = 0; i < 8; ++i) {
+        tmem_ld32(tmem + lane_base + 256 + 32 * i, r);
+        tmem_wait_ld();
+        uint32_t pk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2)
+          pk[j / 2] = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
+        uint4* dst = reinterpret_cast<uint4*>(orow + half * 256 + 32 * i);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (half == 0 && lane == 0) mbar_arrive(o_free);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMma) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 g_enc = nullptr;
+std::once_flag g_enc_once;
+
+bool encode(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+  std::call_once(g_enc_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  if (!g_enc) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(kDqk), rows};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(kDqk) * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kChunk), box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  return g_enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+               es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace ds4a
+
+extern "C" int ds4idx_sparse_attention(const void* q, const void* kv, int64_t kv_rows,
+                                       const int32_t* idx, const int64_t* kv_row0, int64_t T,
+                                       int32_t n_heads, int32_t d_qk, int32_t d_v, int32_t topk,
+                                       float sm_scale, void* out, float* lse, void* stream) {
+  using namespace ds4a;
+  if (n_heads != kH || d_qk != kDqk || d_v != kDv || topk != kK) return DS4IDX_ERR_UNSUPPORTED;
+  if (T < 0 || kv_rows < 1 || kv_rows > 0x7FFFFFFF || T * kH > 0x7FFFFFFF) return DS4IDX_ERR_INVALID_ARG;
+  if (T == 0) return DS4IDX_OK;
+  auto al = [](const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; };
+  if (!q || !kv || !idx || !out || !al(q, 16) || !al(kv, 16) || !al(idx, 4) || !al(out, 16) ||
+      (lse && !al(lse, 4)) || (kv_row0 && !al(kv_row0, 8)) || !(sm_scale > 0.f))
+    return DS4IDX_ERR_INVALID_ARG;
+  CUtensorMap tq, tkv;
+  if (!encode(&tq, q, static_cast<uint64_t>(T) * kH, kH) || !encode(&tkv, kv, kv_rows, 1))
+    return DS4IDX_ERR_INVALID_ARG;
+  SAParams p{};
+  p.idx = idx;
+  p.row0 = kv_row0;
+  p.out = static_cast<uint16_t*>(out);
+  p.lse = lse;
+  p.T = T;
+  p.kv_rows = kv_rows;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  if (cudaFuncSetAttribute(sparse_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return DS4IDX_ERR_CUDA;
+  sparse_attn_kernel<<<static_cast<unsigned>(T), kThreads, kSmemBytes,
+                       static_cast<cudaStream_t>(stream)>>>(tq, tkv, p);
+  if (cudaGetLastError() != cudaSuccess) return DS4IDX_ERR_LAUNCH;
+  ds4w::launch_counter()->fetch_add(1, std::memory_order_relaxed);
+  return DS4IDX_OK;
+}
+
+extern "C" int ds4idx_sparse_attention_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return DS4IDX_ERR_CUDA;
+  uint32_t e = 0;
+  if (cudaMemcpyFromSymbol(&e, ds4a::g_err, sizeof e) != cudaSuccess) return DS4IDX_ERR_CUDA;
+  if (e) {
+    const uint32_t z = 0;
+    cudaMemcpyToSymbol(ds4a::g_err, &z, sizeof z);
+    return DS4IDX_ERR_DEVICE_TIMEOUT;
+  }
+  return DS4IDX_OK;
+}

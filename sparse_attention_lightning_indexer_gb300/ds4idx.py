@@ -35,7 +35,8 @@ EXPORTS = ("ds4idx_create", "ds4idx_score_topk", "ds4idx_score_topk_batched",
            "ds4idx_score_dense_debug", "ds4idx_sync_status", "ds4idx_destroy",
            "ds4idx_status_string", "ds4idx_version", "ds4idx_score_topk_batched_noalloc",
            "ds4idx_kernels_launched", "ds4idx_debug_wait_test", "ds4idx_plan_query",
-           "ds4idx_quantize_keys", "ds4idx_quantize_queries")
+           "ds4idx_quantize_keys", "ds4idx_quantize_queries", "ds4idx_score_topk_varlen",
+           "ds4idx_merge_topk", "ds4idx_sparse_attention", "ds4idx_sparse_attention_status")
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +96,16 @@ def load(path: str | None = None):
         lib.ds4idx_debug_wait_test.restype = ctypes.c_int
         lib.ds4idx_plan_query.argtypes = [i32, i32, i64, i64, vp, i32, vp]
         lib.ds4idx_plan_query.restype = ctypes.c_int
+        lib.ds4idx_score_topk_varlen.argtypes = [vp, i32, vp, vp, vp, vp, vp, i64, vp, vp, i32,
+                                                 i32, vp, vp, i32, vp, vp, vp]
+        lib.ds4idx_score_topk_varlen.restype = ctypes.c_int
+        lib.ds4idx_sparse_attention.argtypes = [vp, vp, i64, vp, vp, i64, i32, i32, i32, i32,
+                                                ctypes.c_float, vp, vp, vp]
+        lib.ds4idx_sparse_attention.restype = ctypes.c_int
+        lib.ds4idx_sparse_attention_status.argtypes = [vp]
+        lib.ds4idx_sparse_attention_status.restype = ctypes.c_int
+        lib.ds4idx_merge_topk.argtypes = [i32, i64, vp, vp, vp, vp, i32, vp, vp, vp]
+        lib.ds4idx_merge_topk.restype = ctypes.c_int
         lib.ds4idx_quantize_keys.argtypes = [vp, i32, i64, vp, i64, vp, vp, i64, vp]
         lib.ds4idx_quantize_keys.restype = ctypes.c_int
         lib.ds4idx_quantize_queries.argtypes = [vp, i32, i64, vp, vp, vp, vp, vp]
@@ -167,6 +178,63 @@ def quantize_queries(q, w, q_codes=None, w_out=None, qscale=None, stream=None):
                                           _ptr(w_out), _ptr(qscale), _stream_ptr(stream)),
            "ds4idx_quantize_queries")
     return q_codes, w_out, qscale
+
+
+def merge_topk(in_idx, in_score, idx_offsets, row0=None, out_idx=None, out_score=None,
+               stream=None):
+    """Merges key-sharded Top-512 lists: in_idx / in_score [L, rows, 512] (shard-local indices,
+    -1 empty), idx_offsets: L host ints (each shard's first key), row0: L host ints or None.
+    Returns (out_idx [rows, 512], out_score [rows, 512])."""
+    L, rows = in_idx.shape[0], in_idx.shape[1]
+    _need(in_idx, (L, rows, TOPK), "in_idx", torch.int32)
+    _need(in_score, (L, rows, TOPK), "in_score", torch.float32)
+    dev = in_idx.device
+    if out_idx is None:
+        out_idx = torch.empty((rows, TOPK), dtype=torch.int32, device=dev)
+    if out_score is None:
+        out_score = torch.empty((rows, TOPK), dtype=torch.float32, device=dev)
+    _need(out_idx, (rows, TOPK), "out_idx", torch.int32)
+    _need(out_score, (rows, TOPK), "out_score", torch.float32)
+    if len(idx_offsets) != L or (row0 is not None and len(row0) != L):
+        raise ValueError("idx_offsets and row0 need one entry per list")
+    offs = (ctypes.c_int64 * L)(*[int(x) for x in idx_offsets])
+    r0 = None if row0 is None else (ctypes.c_int64 * L)(*[int(x) for x in row0])
+    vp = ctypes.c_void_p
+    _check(load().ds4idx_merge_topk(L, rows, _ptr(in_idx), _ptr(in_score), ctypes.cast(offs, vp),
+                                    None if r0 is None else ctypes.cast(r0, vp), TOPK,
+                                    _ptr(out_idx), _ptr(out_score), _stream_ptr(stream)),
+           "ds4idx_merge_topk", "ds4idx_sparse_attention", "ds4idx_sparse_attention_status")
+    return out_idx, out_score
+
+
+SA_HEADS, SA_DQK, SA_DV = 128, 576, 512
+
+
+def sparse_attention(q, kv, idx, sm_scale: float, kv_row0=None, out=None, lse=None, stream=None):
+    """Attention of q [T, 128, 576] (bf16) over the selected rows of kv [R, 576] (bf16):
+    idx [T, 512] int32 positions (-1 empty), kv_row0 [T] int64 or None.
+    Returns (out [T, 128, 512] bf16, lse [T, 128] fp32)."""
+    T, R = q.shape[0], kv.shape[0]
+    _need(q, (T, SA_HEADS, SA_DQK), "q", torch.bfloat16)
+    _need(kv, (R, SA_DQK), "kv", torch.bfloat16)
+    _need(idx, (T, TOPK), "idx", torch.int32)
+    if kv_row0 is not None:
+        _need(kv_row0, (T,), "kv_row0", torch.int64)
+    if out is None:
+        out = torch.empty((T, SA_HEADS, SA_DV), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((T, SA_HEADS), dtype=torch.float32, device=q.device)
+    _need(out, (T, SA_HEADS, SA_DV), "out", torch.bfloat16)
+    _need(lse, (T, SA_HEADS), "lse", torch.float32)
+    _check(load().ds4idx_sparse_attention(_ptr(q), _ptr(kv), R, _ptr(idx), _ptr(kv_row0), T,
+                                          SA_HEADS, SA_DQK, SA_DV, TOPK, float(sm_scale),
+                                          _ptr(out), _ptr(lse), _stream_ptr(stream)),
+           "ds4idx_sparse_attention")
+    return out, lse
+
+
+def sparse_attention_status(stream=None):
+    _check(load().ds4idx_sparse_attention_status(_stream_ptr(stream)), "ds4idx_sparse_attention")
 
 
 def status_string(status: int) -> str:
@@ -298,6 +366,53 @@ class Indexer:
                                                  self.topk, _ptr(out_idx), _ptr(out_score),
                                                  _stream_ptr(stream))
         _check(st, "ds4idx_score_topk_batched")
+        return out_idx, out_score
+
+    def score_topk_varlen(self, q, w, cu_seqlens_q, kcache, kscale, seq_lens, pos_offsets,
+                          kv_start=None, page_table=None, page_size: int = 0, out_idx=None,
+                          out_score=None, stream=None):
+        """Sequences of different lengths in one launch (see include/ds4idx.h).
+
+        q [Q, 64, 128], w [Q, 64]: packed queries, sequence b owning rows
+        cu_seqlens_q[b]..cu_seqlens_q[b+1]-1 (host ints, B + 1 of them). kcache [R, 128] (+ kscale
+        [R]) is the key pool: sequence b's keys start at pool row kv_start[b], or are found through
+        page_table [B, P] (int32, on the device) with page_size keys per page.
+        seq_lens, pos_offsets: B host ints. Returns (out_idx, out_score), [Q, topk].
+        """
+        B = len(seq_lens)
+        Q, R = q.shape[0], kcache.shape[0]
+        q = _codes(q, self.dtype, "q")
+        kcache = _codes(kcache, self.dtype, "kcache")
+        _need(q, (Q, H_I, D_I), "q")
+        _need(w, (Q, H_I), "w", torch.float32)
+        _need(kcache, (R, D_I), "kcache")
+        if kscale is not None:
+            _need(kscale, (R,), "kscale", torch.float32)
+        if len(cu_seqlens_q) != B + 1 or len(pos_offsets) != B:
+            raise ValueError("cu_seqlens_q needs B + 1 entries and pos_offsets B")
+        if page_table is not None:
+            _need(page_table, tuple(page_table.shape), "page_table", torch.int32)
+            if page_table.dim() != 2 or page_table.shape[0] != B:
+                raise ValueError("page_table must be [B, pages_per_seq]")
+        dev = q.device
+        if out_idx is None:
+            out_idx = torch.empty((Q, self.topk), dtype=torch.int32, device=dev)
+        if out_score is None:
+            out_score = torch.empty((Q, self.topk), dtype=torch.float32, device=dev)
+        _need(out_idx, (Q, self.topk), "out_idx", torch.int32)
+        _need(out_score, (Q, self.topk), "out_score", torch.float32)
+        I64 = ctypes.c_int64
+        cu = (I64 * (B + 1))(*[int(x) for x in cu_seqlens_q])
+        sl = (I64 * B)(*[int(x) for x in seq_lens])
+        po = (I64 * B)(*[int(x) for x in pos_offsets])
+        ks = None if kv_start is None else (I64 * B)(*[int(x) for x in kv_start])
+        vp = ctypes.c_void_p
+        st = self._lib.ds4idx_score_topk_varlen(
+            self._h, B, _ptr(q), _ptr(w), ctypes.cast(cu, vp), _ptr(kcache), _ptr(kscale), R,
+            None if ks is None else ctypes.cast(ks, vp), _ptr(page_table), int(page_size),
+            0 if page_table is None else int(page_table.shape[1]), ctypes.cast(sl, vp),
+            ctypes.cast(po, vp), self.topk, _ptr(out_idx), _ptr(out_score), _stream_ptr(stream))
+        _check(st, "ds4idx_score_topk_varlen")
         return out_idx, out_score
 
     def score_dense_debug(self, q, w, kcache, kscale=None, pos_offset: int = 0, out=None,

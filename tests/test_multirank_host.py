@@ -32,7 +32,7 @@ def test_two_rank_aggregate_takes_the_slowest_rank():
     world = 2
     port = _free_port()
     times = [40.0, 50.0]  # ms
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, port, times, out), nprocs=world, join=True)
         res = dict(out)
