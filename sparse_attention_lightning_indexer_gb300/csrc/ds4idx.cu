@@ -138,9 +138,18 @@ size_t plan_counters(const Plan& pl, int64_t B) {
 
 template <int DT, int NQ, bool DENSE>
 cudaError_t set_smem_attr() {
+  using C = KCfg<DT, NQ, DENSE>;
+  if constexpr (C::kRegW) {
+    // The kernel moves registers between its warpgroups (setmaxnreg); that exchange completes
+    // only if each thread was launched with exactly kRegLaunch registers. Refuse to run a build
+    // whose register count differs rather than risk a kernel that waits forever.
+    cudaFuncAttributes fa{};
+    const cudaError_t e = cudaFuncGetAttributes(&fa, indexer_kernel<DT, NQ, DENSE>);
+    if (e != cudaSuccess) return e;
+    if (fa.numRegs != C::kRegLaunch) return cudaErrorInvalidKernelImage;
+  }
   return cudaFuncSetAttribute(indexer_kernel<DT, NQ, DENSE>,
-                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              KCfg<DT, NQ, DENSE>::kSmemBytes);
+                              cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes);
 }
 
 // Tensor map over `rows` rows of 128 elements per batch entry: dims {128, rows, B}.

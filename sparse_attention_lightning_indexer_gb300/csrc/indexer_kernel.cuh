@@ -168,7 +168,18 @@ struct KCfg {
   static constexpr int kTmaWarp = kEpiWarps;
   static constexpr int kMmaWarp = kEpiWarps + 1;
   static constexpr int kSelWarp0 = kEpiWarps + 2;
-  static constexpr int kWarps = kEpiWarps + 2 + kSelectors;
+  // Four-query scoring CTAs keep the head weights of their two queries in registers (128 per
+  // epilogue thread), so the hot loop issues no shared-memory loads beside the tensor core's
+  // operand reads. The CTA is 4 whole warpgroups (two idle warps complete the last one) launched
+  // at kRegLaunch registers per thread; after set-up the two epilogue warpgroups take kRegEpi
+  // and the other two give up to kRegOther (setmaxnreg; 2 * kRegLaunch = kRegEpi + kRegOther, so
+  // the exchange always completes), and before the end-of-kernel selection all return to
+  // kRegLaunch. The debug export keeps the shared-memory weights: it runs the same arithmetic.
+  static constexpr bool kRegW = NQ == 4 && !DENSE;
+  static constexpr int kRegLaunch = 128, kRegEpi = 168, kRegOther = 88;
+  static_assert(kRegEpi + kRegOther == 2 * kRegLaunch, "register exchange is balanced");
+  static constexpr int kWarps = kRegW ? 16 : kEpiWarps + 2 + kSelectors;
+  static_assert(!kRegW || kWarps >= kEpiWarps + 2 + kSelectors, "every role has a warp");
   static constexpr int kThreads = 32 * kWarps;
   static constexpr uint32_t kTmemCols = 512;
   static_assert(kAccBufs * kN == 512 && kAccBufs >= 2, "accumulators tile the TMEM columns");
@@ -894,7 +905,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  if (warp == C::kTmaWarp) {
+  // ---- warp roles
+  auto tma_role = [&]() {
     // ================= TMA producer
     if (lane == 0 && n_tiles > 0) {
       mbar_arrive_expect_tx(qfull, C::kQBytes);
@@ -936,7 +948,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         mbar_drain(&full[j % C::kStages], (j / C::kStages) & 1);
       mbar_drain(qfull, 0);
     }
-  } else if (warp == C::kMmaWarp) {
+  };
+  auto mma_role = [&]() {
     // ================= MMA issuer (one thread)
     if (lane == 0 && n_tiles > 0) {
       int it = 0;
@@ -974,7 +987,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp < C::kEpiWarps) {
+  };
+  auto epi_role = [&]() {
     // ================= epilogue: TMEM -> ReLU . w -> per-key score
     const int quad = warp & 3;
     const int grp = warp >> 2;
@@ -993,6 +1007,11 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       return row < p.pool_rows ? __ldg(p.kscale + row) : 0.f;
     };
     float ks_next0 = 1.f, ks_next1 = 1.f;
+    float wr[C::kRegW ? C::kQPerGroup * kHeads : 1];        // the group's head weights
+    if constexpr (C::kRegW) {
+#pragma unroll
+      for (int i = 0; i < C::kQPerGroup * kHeads; ++i) wr[i] = sW[q0 * kHeads + i];
+    }
     uint32_t own_cand = 0u;                                  // buffered mode: keys listed
     uint16_t* own_list = s_cand + warp * C::kCandSeg;        // buffered mode: their offsets
     if (DT == kDtFp8) {
@@ -1015,6 +1034,49 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       tc_fence_after();
       if (!DENSE && !buffered) {
         if (!mbar_wait_warp<C::kWaitHint>(&sempty[sb], sph ^ 1u, s_abort, p.err, p.wait_ns)) break;
+      }
+      if constexpr (C::kRegW) {
+        // Weights in registers: 16-column TMEM chunks (8 per tile), double-buffered.
+        constexpr int kChunks16 = 4 * C::kQPerGroup;
+        const uint32_t col0 = tmem + lane_base + static_cast<uint32_t>(acc * C::kN + q0 * kHeads);
+        uint32_t rb[2][16];
+        tmem_ld16(col0, rb[0]);
+        tmem_wait_ld();
+        uint64_t acc01 = 0ull, acc23 = 0ull;
+#pragma unroll
+        for (int c = 0; c < kChunks16; ++c) {
+          if (c + 1 < kChunks16) tmem_ld16(col0 + 16 * (c + 1), rb[(c + 1) & 1]);
+          const int lq = c / 4;  // query of the group
+          const uint32_t* r = rb[c & 1];
+#pragma unroll
+          for (int h4 = 0; h4 < 4; ++h4) {
+            const int wi = lq * kHeads + (c % 4) * 16 + 4 * h4;
+            const float x0 = fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f);
+            const float x1 = fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f);
+            const float x2 = fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f);
+            const float x3 = fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f);
+            acc01 = fma_f32x2(pack_f32x2(x0, x1), pack_f32x2(wr[wi], wr[wi + 1]), acc01);
+            acc23 = fma_f32x2(pack_f32x2(x2, x3), pack_f32x2(wr[wi + 2], wr[wi + 3]), acc23);
+          }
+          if (c % 4 == 3) {  // all 64 heads of query q0 + lq reduced
+            float a0, a1, a2, a3;
+            unpack_f32x2(acc01, a0, a1);
+            unpack_f32x2(acc23, a2, a3);
+            acc01 = 0ull;
+            acc23 = 0ull;
+            float score = (a0 + a1) + (a2 + a3);
+            if (DT == kDtFp8) score *= ks;
+            sScore[(sb * NQ + q0 + lq) * kTileKeys + quad * 32 + lane] = score;
+          }
+          if (c + 1 < kChunks16) tmem_wait_ld();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[acc]);
+          mbar_arrive(&sfull[sb]);
+        }
+        continue;
       }
       // The warp's TMEM reads are 2 * kQPerGroup chunks of 32 head columns. Chunk c+1 is
       // requested before chunk c is reduced, so each load's latency hides behind arithmetic
@@ -1110,7 +1172,25 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       }
     }
     if (buffered && lane == 0) s_ncand[warp] = own_cand;
-  } else if (!DENSE) {
+  };
+  // A selector warp's last step (one CTA, no key split): its pool back to exactly the 512 best,
+  // sorted in registers, best first, and written as the query's output row.
+  auto sel_finish = [&](int sidx, int n) {
+    uint64_t* pool = sPool + sidx * C::kPool;
+    const int64_t t = t0 + sidx / C::kSelPerQuery;
+    if (n > kTopK) n = (select_compact<kTopK>(pool, n, sHist + sidx * 256, lane), kTopK);
+    __syncwarp();
+    constexpr int R = kTopK / 32;
+    uint64_t v[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const int i = lane * R + r;
+      v[r] = i < n ? pool[i] : 0ull;
+    }
+    warp_sort_desc<R>(v, lane);
+    if (t < sd.T && !*s_abort) write_output<R>(p, sd.q_row0 + t, v, lane);
+  };
+  auto sel_role = [&]() {
     // ================= selectors
     const int sidx = warp - C::kSelWarp0;
     const int q = sidx / C::kSelPerQuery;
@@ -1161,19 +1241,27 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       // Finished with a CTA-wide select after the role loops (every warp helps).
       if (lane == 0) s_pool_n[sidx] = static_cast<uint32_t>(n);
     } else {
-      if (n > kTopK) n = (select_compact<kTopK>(pool, n, hist, lane), kTopK);
-      __syncwarp();
-      // Final order: sort the (at most 512) survivors in registers, best first.
-      constexpr int R = kTopK / 32;
-      uint64_t v[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const int i = lane * R + r;
-        v[r] = i < n ? pool[i] : 0ull;
-      }
-      warp_sort_desc<R>(v, lane);
-      if (valid && !*s_abort) write_output<R>(p, sd.q_row0 + t, v, lane);
+      sel_finish(sidx, n);
     }
+  };
+  if constexpr (C::kRegW) {
+    // whole warpgroups change their register allocation at the top of their branch
+    if (warp < C::kEpiWarps) {
+      setmaxnreg_inc<C::kRegEpi>();
+      epi_role();
+      setmaxnreg_dec<C::kRegLaunch>();
+    } else {
+      setmaxnreg_dec<C::kRegOther>();
+      if (warp == C::kTmaWarp) tma_role();
+      else if (warp == C::kMmaWarp) mma_role();
+      else if (warp < C::kSelWarp0 + C::kSelectors) sel_role();
+      setmaxnreg_inc<C::kRegLaunch>();
+    }
+  } else {
+    if (warp == C::kTmaWarp) tma_role();
+    else if (warp == C::kMmaWarp) mma_role();
+    else if (warp < C::kEpiWarps) epi_role();
+    else if (!DENSE && warp < C::kSelWarp0 + C::kSelectors) sel_role();
   }
 
   __syncwarp();

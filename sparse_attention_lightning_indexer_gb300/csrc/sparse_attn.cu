@@ -173,9 +173,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducer) {
     // ---------------- gathers
+    int issued_a = 0, issued_v = 0;
     for (int c = 0; c < kNChunks; ++c) {
       const int st = c & 1;
       if (!mbar_wait_warp(&a_empty[st], ((c >> 1) & 1) ^ 1u, s_abort, err)) break;
+      issued_a = c + 1;
       uint8_t* base = smem + st * kAStageBytes;
       if (lane == 0) {
         mbar_arrive_expect_tx(&a_full[st], kAStageBytes);
@@ -191,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = 0; i < 2 * (kK / kVKeys); ++i) {
         const int half = i / (kK / kVKeys), kc = i % (kK / kVKeys), st = i & 1;
         if (!mbar_wait_warp(&v_empty[st], ((i >> 1) & 1) ^ 1u, s_abort, err)) break;
+        issued_v = i + 1;
         uint8_t* base = smem + kOffV + st * kVStageBytes;
         if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kVStageBytes);
         __syncwarp();
@@ -202,11 +205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
-    // never exit with gathers in flight
-    for (int st = 0; st < 2; ++st) {
-      mbar_drain(&a_full[st], 0u);
-      mbar_drain(&v_full[st], 1u);
-    }
+    // never exit with gathers in flight: wait for the last load issued on each stage
+    for (int j = issued_a > 2 ? issued_a - 2 : 0; j < issued_a; ++j)
+      mbar_drain(&a_full[j & 1], (j >> 1) & 1);
+    for (int j = issued_v > 2 ? issued_v - 2 : 0; j < issued_v; ++j)
+      mbar_drain(&v_full[j & 1], (j >> 1) & 1);
   } else if (warp == kMma) {
     // ---------------- MMA issue (one thread)
     if (lane == 0) {

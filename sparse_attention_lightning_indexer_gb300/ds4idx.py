@@ -203,7 +203,7 @@ def merge_topk(in_idx, in_score, idx_offsets, row0=None, out_idx=None, out_score
     _check(load().ds4idx_merge_topk(L, rows, _ptr(in_idx), _ptr(in_score), ctypes.cast(offs, vp),
                                     None if r0 is None else ctypes.cast(r0, vp), TOPK,
                                     _ptr(out_idx), _ptr(out_score), _stream_ptr(stream)),
-           "ds4idx_merge_topk", "ds4idx_sparse_attention", "ds4idx_sparse_attention_status")
+           "ds4idx_merge_topk")
     return out_idx, out_score
 
 
