@@ -239,6 +239,47 @@ __device__ __forceinline__ void write_output(const KParams& p, int64_t row,
   }
 }
 
+// The weighted head sum of one query for one key, sum_j w_j * max(0, x_j), accumulated four
+// heads at a time in packed fp32x2 FMAs. FP8 scoring applies the ReLU directly (a max per head on
+// the ALU pipe beside a packed FMA per two heads). bf16 scoring, whose epilogue runs beside a
+// tensor core that is busier per key, uses max(0, x) = (x + |x|) / 2 and accumulates w.x and
+// w.|x| separately, all on the FMA pipe: the same value up to fp32 rounding of the two sums.
+// Every kernel of a dtype (Top-k and dense debug) uses the same helper, so their scores agree
+// bit for bit.
+template <int DT>
+struct HeadSum {
+  uint64_t a = 0ull, b = 0ull, c = 0ull, d = 0ull;
+  __device__ __forceinline__ void add4(const uint32_t* r, float w0, float w1, float w2, float w3) {
+    const float x0 = __uint_as_float(r[0]), x1 = __uint_as_float(r[1]);
+    const float x2 = __uint_as_float(r[2]), x3 = __uint_as_float(r[3]);
+    const uint64_t w01 = pack_f32x2(w0, w1), w23 = pack_f32x2(w2, w3);
+    if constexpr (DT == kDtFp8) {
+      a = fma_f32x2(pack_f32x2(fmaxf(x0, 0.f), fmaxf(x1, 0.f)), w01, a);
+      b = fma_f32x2(pack_f32x2(fmaxf(x2, 0.f), fmaxf(x3, 0.f)), w23, b);
+    } else {
+      a = fma_f32x2(pack_f32x2(x0, x1), w01, a);
+      b = fma_f32x2(pack_f32x2(fabsf(x0), fabsf(x1)), w01, b);
+      c = fma_f32x2(pack_f32x2(x2, x3), w23, c);
+      d = fma_f32x2(pack_f32x2(fabsf(x2), fabsf(x3)), w23, d);
+    }
+  }
+  // The sum, and the accumulators cleared for the next query.
+  __device__ __forceinline__ float take() {
+    float a0, a1, b0, b1;
+    unpack_f32x2(a, a0, a1);
+    unpack_f32x2(b, b0, b1);
+    float s = (a0 + a1) + (b0 + b1);
+    if constexpr (DT != kDtFp8) {
+      float c0, c1, d0, d1;
+      unpack_f32x2(c, c0, c1);
+      unpack_f32x2(d, d0, d1);
+      s = 0.5f * (s + ((c0 + c1) + (d0 + d1)));
+    }
+    a = b = c = d = 0ull;
+    return s;
+  }
+};
+
 // Bucket positions for a bin-grouped slot list (one warp): bucket r < nb holds bin whi - r, the
 // last bucket (r = nb) every word below the window. cur[r] receives the number of words in
 // buckets before r; cnt(bin) gives the exact count of each window bin.
@@ -1042,7 +1083,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         uint32_t rb[2][16];
         tmem_ld16(col0, rb[0]);
         tmem_wait_ld();
-        uint64_t acc01 = 0ull, acc23 = 0ull;
+        HeadSum<DT> hs;
 #pragma unroll
         for (int c = 0; c < kChunks16; ++c) {
           if (c + 1 < kChunks16) tmem_ld16(col0 + 16 * (c + 1), rb[(c + 1) & 1]);
@@ -1051,20 +1092,10 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
 #pragma unroll
           for (int h4 = 0; h4 < 4; ++h4) {
             const int wi = lq * kHeads + (c % 4) * 16 + 4 * h4;
-            const float x0 = fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f);
-            const float x1 = fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f);
-            const float x2 = fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f);
-            const float x3 = fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f);
-            acc01 = fma_f32x2(pack_f32x2(x0, x1), pack_f32x2(wr[wi], wr[wi + 1]), acc01);
-            acc23 = fma_f32x2(pack_f32x2(x2, x3), pack_f32x2(wr[wi + 2], wr[wi + 3]), acc23);
+            hs.add4(r + 4 * h4, wr[wi], wr[wi + 1], wr[wi + 2], wr[wi + 3]);
           }
           if (c % 4 == 3) {  // all 64 heads of query q0 + lq reduced
-            float a0, a1, a2, a3;
-            unpack_f32x2(acc01, a0, a1);
-            unpack_f32x2(acc23, a2, a3);
-            acc01 = 0ull;
-            acc23 = 0ull;
-            float score = (a0 + a1) + (a2 + a3);
+            float score = hs.take();
             if (DT == kDtFp8) score *= ks;
             sScore[(sb * NQ + q0 + lq) * kTileKeys + quad * 32 + lane] = score;
           }
@@ -1086,31 +1117,20 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       uint32_t rb[2][32];
       tmem_ld32(col0, rb[0]);
       tmem_wait_ld();
-      uint64_t acc01 = 0ull, acc23 = 0ull;
+      HeadSum<DT> hs;
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
         if (c + 1 < kChunks) tmem_ld32(col0 + 32 * (c + 1), rb[(c + 1) & 1]);
         const int q = q0 + c / 2;
-        // Four accumulator chains (heads = 0, 1, 2, 3 mod 4), two per packed fp32x2 FMA.
         const float4* w4 = reinterpret_cast<const float4*>(sW + q * kHeads + (c & 1) * 32);
         const uint32_t* r = rb[c & 1];
 #pragma unroll
         for (int h4 = 0; h4 < 8; ++h4) {
           const float4 wv = w4[h4];
-          const float x0 = fmaxf(__uint_as_float(r[4 * h4 + 0]), 0.f);
-          const float x1 = fmaxf(__uint_as_float(r[4 * h4 + 1]), 0.f);
-          const float x2 = fmaxf(__uint_as_float(r[4 * h4 + 2]), 0.f);
-          const float x3 = fmaxf(__uint_as_float(r[4 * h4 + 3]), 0.f);
-          acc01 = fma_f32x2(pack_f32x2(x0, x1), pack_f32x2(wv.x, wv.y), acc01);
-          acc23 = fma_f32x2(pack_f32x2(x2, x3), pack_f32x2(wv.z, wv.w), acc23);
+          hs.add4(r + 4 * h4, wv.x, wv.y, wv.z, wv.w);
         }
         if (c & 1) {  // both halves of query q reduced
-          float a0, a1, a2, a3;
-          unpack_f32x2(acc01, a0, a1);
-          unpack_f32x2(acc23, a2, a3);
-          acc01 = 0ull;
-          acc23 = 0ull;
-          float score = (a0 + a1) + (a2 + a3);
+          float score = hs.take();
           if (DT == kDtFp8) score *= ks;
           if (DENSE) {
             const int64_t t = t0 + q;

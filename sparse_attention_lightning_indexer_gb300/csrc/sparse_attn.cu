@@ -8,17 +8,19 @@
 //     lse[t,h] = log sum_j exp(s_j).
 //
 // One CTA per token, all 128 heads (heads = TMEM lanes, so each softmax row lives in one
-// thread). Warps 0-3 are the softmax / output warps (thread h owns head h), warp 4 gathers rows
-// with TMA (tile::gather4 of 4 rows x 64 dims per instruction), warp 5 issues tcgen05.mma.
+// thread). Warps 0-3 are the softmax / output warps (thread h owns head h), warps 4-7 gather the
+// selected rows with cp.async (eight threads per 128-byte row segment, so every warp instruction
+// moves four whole segments) into the 128-byte-swizzled operand layout, warp 8 issues tcgen05.mma.
 //   A  S[128 heads x 512 keys] = Q K^T accumulates over 9 chunks of 64 dims: per chunk a Q
 //      chunk (tiled TMA) and the chunk of all 512 gathered key rows; 4 MMAs of N = 128 keys per
 //      16-dim step into TMEM columns 0..511.
 //   B  two passes over S in TMEM: the row maximum, then p = exp2(s * scale * log2 e - max),
 //      summed in fp32 and stored as bf16 into shared memory in the K-major 128-byte-swizzled
 //      layout of an MMA A operand (8 blocks of 64 keys).
-//   C  O[128 x 512] = P V in two halves of 256 value dims (TMEM columns 256..511, free once S is
-//      read): V chunks of 64 keys x 256 dims are gathered again and fed as an MN-major B operand.
-//      The output warps scale each half by 1 / sum and store it as bf16.
+//   C  O[128 x 512] = P V in two halves of 256 value dims (TMEM columns 0..255 and 256..511, free
+//      once S is read, so the second half's MMAs run while the first half is stored): V chunks of
+//      64 keys x 256 dims are gathered again and fed as an MN-major B operand. The output warps
+//      scale each half by 1 / sum and store it as bf16.
 // Shared memory: phase A's two 80 KB stages and phase C's P (128 KB) + two 32 KB V stages share
 // one 192 KB region (the phases of a token never overlap).
 #include <cuda.h>
@@ -58,11 +60,12 @@ static_assert(2 * kAStageBytes <= kRegion, "phase A stages fit the shared region
 constexpr int kOffRows = kRegion;                   // int32 gather rows [512]
 constexpr int kOffMask = kOffRows + kK * 4;         // uint32 validity words [16]
 constexpr int kOffBars = kOffMask + 64;
-constexpr int kNumBars = 2 + 2 + 1 + 1 + 2 + 2 + 1 + 1;
+constexpr int kNumBars = 2 + 2 + 1 + 1 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
-constexpr int kThreads = 6 * 32;
-constexpr int kProducer = 4, kMma = 5;
+constexpr int kProducer0 = 4, kProducers = 4, kMma = 8;
+constexpr int kThreads = (kMma + 1) * 32;
+constexpr int kProducerThreads = kProducers * 32;
 // B operand of P.V: V chunk rows are keys (the K dimension), 64 value dims per 128-byte row
 // (the N dimension): an MN-major operand. Atoms of 8 keys x 64 dims (1 KB) repeat every 1 KB
 // along K and every kVKeys * 128 bytes along N.
@@ -109,6 +112,12 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
   d |= static_cast<uint64_t>(2u) << 61;
   return d;
 }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   uint32_t d;
   asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
@@ -116,8 +125,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q,
-                       const __grid_constant__ CUtensorMap tmap_kv, const __grid_constant__ SAParams p) {
+    sparse_attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const uint16_t* __restrict__ kv,
+                       const __grid_constant__ SAParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -131,7 +140,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* v_full = bars + 6;    // [2]
   uint64_t* v_empty = bars + 8;   // [2]
   uint64_t* o_ready = bars + 10;
-  uint64_t* o_free = bars + 11;
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + kOffMisc);
   volatile uint32_t* s_abort = reinterpret_cast<volatile uint32_t*>(smem + kOffMisc + 4);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -139,15 +147,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&a_full[i], 1);
+      mbar_init(&a_full[i], kProducerThreads + 1);  // every gather thread + the Q chunk's TMA
       mbar_init(&a_empty[i], 1);
-      mbar_init(&v_full[i], 1);
+      mbar_init(&v_full[i], kProducerThreads);
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_ready, 1);
     mbar_init(p_ready, 4);
     mbar_init(o_ready, 1);
-    mbar_init(o_free, 4);
     *s_abort = 0u;
     fence_mbar_init();
   }
@@ -171,45 +178,69 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   uint32_t* err = &g_err;
 
-  if (warp == kProducer) {
-    // ---------------- gathers
-    int issued_a = 0, issued_v = 0;
+  if (warp >= kProducer0 && warp < kProducer0 + kProducers) {
+    // ---------------- gathers: each thread copies its 16-byte pieces, waits for them one stage
+    // later (cp.async groups), makes them visible to the tensor core (proxy fence) and arrives.
+    const int pt = threadIdx.x - kProducer0 * 32;  // 0..127
+    const int pw = pt >> 5;
+    const int seg = lane & 7, sub = lane >> 3;      // K rows: 8 threads per 128-byte segment
+    int issued_q = 0;
+    bool ok = true;
     for (int c = 0; c < kNChunks; ++c) {
       const int st = c & 1;
-      if (!mbar_wait_warp(&a_empty[st], ((c >> 1) & 1) ^ 1u, s_abort, err)) break;
-      issued_a = c + 1;
+      if (!(ok = mbar_wait_warp(&a_empty[st], ((c >> 1) & 1) ^ 1u, s_abort, err))) break;
       uint8_t* base = smem + st * kAStageBytes;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(&a_full[st], kAStageBytes);
+      if (pt == 0) {
+        mbar_arrive_expect_tx(&a_full[st], kH * 128);
         tma_load_2d(base, &tmap_q, &a_full[st], c * kChunk, static_cast<int32_t>(t * kH));
+        issued_q = c + 1;
       }
-      __syncwarp();
-      for (int g = lane; g < kK / 4; g += 32)
-        gather4(base + kH * 128 + g * 512, &tmap_kv, &a_full[st], c * kChunk, s_rows[4 * g],
-                s_rows[4 * g + 1], s_rows[4 * g + 2], s_rows[4 * g + 3]);
+      uint8_t* kbase = base + kH * 128;
+      for (int i = 0; i < kK / (4 * kProducers); ++i) {
+        const int r = (i * kProducers + pw) * 4 + sub;  // key row 0..511
+        cp_async16(kbase + r * 128 + ((seg ^ (r & 7)) * 16),
+                   kv + static_cast<int64_t>(s_rows[r]) * kDqk + c * kChunk + seg * 8);
+      }
+      cp_async_commit();
+      if (c > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        mbar_arrive(&a_full[(c - 1) & 1]);
+      }
     }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    if (ok) mbar_arrive(&a_full[(kNChunks - 1) & 1]);
     // phase C reuses the region: wait until every phase-A MMA has completed
-    if (mbar_wait_warp(s_ready, 0u, s_abort, err)) {
+    if (ok && mbar_wait_warp(s_ready, 0u, s_abort, err)) {
       for (int i = 0; i < 2 * (kK / kVKeys); ++i) {
         const int half = i / (kK / kVKeys), kc = i % (kK / kVKeys), st = i & 1;
-        if (!mbar_wait_warp(&v_empty[st], ((i >> 1) & 1) ^ 1u, s_abort, err)) break;
-        issued_v = i + 1;
+        if (!(ok = mbar_wait_warp(&v_empty[st], ((i >> 1) & 1) ^ 1u, s_abort, err))) break;
         uint8_t* base = smem + kOffV + st * kVStageBytes;
-        if (lane == 0) mbar_arrive_expect_tx(&v_full[st], kVStageBytes);
-        __syncwarp();
-        for (int x = lane; x < 4 * (kVKeys / 4); x += 32) {
-          const int nb = x / (kVKeys / 4), g = x % (kVKeys / 4);
-          const int j = kc * kVKeys + 4 * g;
-          gather4(base + nb * kVStrideN + g * 512, &tmap_kv, &v_full[st], half * 256 + nb * 64,
-                  s_rows[j], s_rows[j + 1], s_rows[j + 2], s_rows[j + 3]);
+        // V rows: one warp instruction copies one row's 512 bytes (32 x 16)
+        for (int j = 0; j < kVKeys / kProducers; ++j) {
+          const int r = j * kProducers + pw;  // 0..63 within the chunk
+          const int nb = lane >> 3, cc = lane & 7;
+          cp_async16(base + nb * kVStrideN + r * 128 + ((cc ^ (r & 7)) * 16),
+                     kv + static_cast<int64_t>(s_rows[kc * kVKeys + r]) * kDqk + half * 256 + lane * 8);
+        }
+        cp_async_commit();
+        if (i > 0) {
+          cp_async_wait<1>();
+          fence_proxy_async_smem();
+          mbar_arrive(&v_full[(i - 1) & 1]);
+        }
+        if (i == 2 * (kK / kVKeys) - 1) {
+          cp_async_wait<0>();
+          fence_proxy_async_smem();
+          mbar_arrive(&v_full[i & 1]);
         }
       }
     }
-    // never exit with gathers in flight: wait for the last load issued on each stage
-    for (int j = issued_a > 2 ? issued_a - 2 : 0; j < issued_a; ++j)
-      mbar_drain(&a_full[j & 1], (j >> 1) & 1);
-    for (int j = issued_v > 2 ? issued_v - 2 : 0; j < issued_v; ++j)
-      mbar_drain(&v_full[j & 1], (j >> 1) & 1);
+    cp_async_wait<0>();  // never exit with copies in flight
+    if (pt == 0)
+      for (int j = issued_q > 2 ? issued_q - 2 : 0; j < issued_q; ++j)
+        mbar_drain(&a_full[j & 1], (j >> 1) & 1);
   } else if (warp == kMma) {
     // ---------------- MMA issue (one thread)
     if (lane == 0) {
@@ -234,15 +265,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t pa = smem_u32(smem + kOffP);
       for (int i = 0; ok && i < 2 * (kK / kVKeys); ++i) {
         const int half = i / (kK / kVKeys), kc = i % (kK / kVKeys), st = i & 1;
-        if (half == 1 && kc == 0) {
-          if (!(ok = mbar_wait(o_free, 0u, s_abort, err))) break;
-          tc_fence_after();
-        }
         if (!(ok = mbar_wait(&v_full[st], (i >> 1) & 1, s_abort, err))) break;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kOffV + st * kVStageBytes);
         for (int ks = 0; ks < kVKeys / 16; ++ks)
-          mma_bf16(tmem + 256, smem_desc_sw128(pa + kc * (kH * 128) + ks * 32),
+          mma_bf16(tmem + 256 * half, smem_desc_sw128(pa + kc * (kH * 128) + ks * 32),
                    smem_desc_mn_sw128(vb + ks * 16 * 128, kVStrideN, kVStrideK), kIdescO,
                    (kc | ks) ? 1u : 0u);
         mma_commit(&v_empty[st]);
@@ -261,19 +288,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_wait_warp(s_ready, 0u, s_abort, err);
     tc_fence_after();
     if (ok) {
-      uint32_t r[32];
+      // Two passes over S, each reading 32-column chunks with the next chunk's load in flight.
+      uint32_t rb[2][32];
+      tmem_ld32(tmem + lane_base, rb[0]);
+      tmem_wait_ld();
+#pragma unroll 2
       for (int i = 0; i < kK / 32; ++i) {
-        tmem_ld32(tmem + lane_base + 32 * i, r);
-        tmem_wait_ld();
+        if (i + 1 < kK / 32) tmem_ld32(tmem + lane_base + 32 * (i + 1), rb[(i + 1) & 1]);
+        const uint32_t* r = rb[i & 1];
         const uint32_t vm = s_mask[i];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
           if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]) * p.scale_log2);
+        tmem_wait_ld();
       }
       const float mm = m == -__int_as_float(0x7f800000) ? 0.f : m;
+      tmem_ld32(tmem + lane_base, rb[0]);
+      tmem_wait_ld();
+#pragma unroll 2
       for (int i = 0; i < kK / 32; ++i) {
-        tmem_ld32(tmem + lane_base + 32 * i, r);
-        tmem_wait_ld();
+        if (i + 1 < kK / 32) tmem_ld32(tmem + lane_base + 32 * (i + 1), rb[(i + 1) & 1]);
+        const uint32_t* r = rb[i & 1];
         const uint32_t vm = s_mask[i];
         uint32_t pk[16];
 #pragma unroll
@@ -291,6 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           *reinterpret_cast<uint4*>(row + ((cc ^ (h & 7)) * 16)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
+        tmem_wait_ld();
       }
     }
     fence_proxy_async_smem();  // P (generic writes) before the MMAs that read it
@@ -304,10 +340,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int half = 0; ok && half < 2; ++half) {
       if (!(ok = mbar_wait_warp(o_ready, static_cast<uint32_t>(half), s_abort, err))) break;
       tc_fence_after();
-      uint32_t r[32];
+      uint32_t rb[2][32];
+      const uint32_t ocol = tmem + lane_base + 256 * half;
+      tmem_ld32(ocol, rb[0]);
+      tmem_wait_ld();
       for (int i = 0; i < 8; ++i) {
-        tmem_ld32(tmem + lane_base + 256 + 32 * i, r);
-        tmem_wait_ld();
+        if (i + 1 < 8) tmem_ld32(ocol + 32 * (i + 1), rb[(i + 1) & 1]);
+        const uint32_t* r = rb[i & 1];
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2)
@@ -315,10 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint4* dst = reinterpret_cast<uint4*>(orow + half * 256 + 32 * i);
 #pragma unroll
         for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        tmem_wait_ld();
       }
-      tc_fence_before();
-      __syncwarp();
-      if (half == 0 && lane == 0) mbar_arrive(o_free);
     }
   }
   __syncwarp();
@@ -366,9 +403,8 @@ extern "C" int ds4idx_sparse_attention(const void* q, const void* kv, int64_t kv
   if (!q || !kv || !idx || !out || !al(q, 16) || !al(kv, 16) || !al(idx, 4) || !al(out, 16) ||
       (lse && !al(lse, 4)) || (kv_row0 && !al(kv_row0, 8)) || !(sm_scale > 0.f))
     return DS4IDX_ERR_INVALID_ARG;
-  CUtensorMap tq, tkv;
-  if (!encode(&tq, q, static_cast<uint64_t>(T) * kH, kH) || !encode(&tkv, kv, kv_rows, 1))
-    return DS4IDX_ERR_INVALID_ARG;
+  CUtensorMap tq;
+  if (!encode(&tq, q, static_cast<uint64_t>(T) * kH, kH)) return DS4IDX_ERR_INVALID_ARG;
   SAParams p{};
   p.idx = idx;
   p.row0 = kv_row0;
@@ -381,7 +417,7 @@ extern "C" int ds4idx_sparse_attention(const void* q, const void* kv, int64_t kv
                            kSmemBytes) != cudaSuccess)
     return DS4IDX_ERR_CUDA;
   sparse_attn_kernel<<<static_cast<unsigned>(T), kThreads, kSmemBytes,
-                       static_cast<cudaStream_t>(stream)>>>(tq, tkv, p);
+                       static_cast<cudaStream_t>(stream)>>>(tq, static_cast<const uint16_t*>(kv), p);
   if (cudaGetLastError() != cudaSuccess) return DS4IDX_ERR_LAUNCH;
   ds4w::launch_counter()->fetch_add(1, std::memory_order_relaxed);
   return DS4IDX_OK;
