@@ -12,7 +12,9 @@
 //                thread, for its queries, and reduces the 64 head columns of each query
 //                thread-locally (ReLU, * w, sum) with packed fp32x2 FMAs, so the T x S score
 //                matrix never leaves the SM; two warps per lane quadrant hide TMEM latency
-//                (they split the queries, or take alternate tiles when NQ = 1);
+//                (they split the queries, or take alternate tiles when NQ = 1). With NQ = 4
+//                the CTA is four warpgroups and the two epilogue warpgroups hold their queries'
+//                head weights in registers (setmaxnreg moves registers to them);
 //   TMA          Q block once, then 128-key K tiles into a ring of stages;
 //   MMA          TMEM owner and MMA issuer: per key tile, D[128 keys, NQ*64 (query, head)]
 //                = K_tile . Q_block^T on tcgen05 into one of the TMEM accumulators (all 512

@@ -7,10 +7,12 @@
 //     s_j = scale * q[t,h,:] . kv[j,:],   o[t,h,:] = sum_j softmax(s)_j kv[j, 0:512],
 //     lse[t,h] = log sum_j exp(s_j).
 //
-// One CTA per token, all 128 heads (heads = TMEM lanes, so each softmax row lives in one
-// thread). Warps 0-3 are the softmax / output warps (thread h owns head h), warps 4-7 gather the
+// One CTA per token, all 128 heads (heads = TMEM lanes, so each softmax row lives in the two
+// threads of its lane). Warps 0-3 and 8-11 are the softmax / output warps (two per TMEM lane
+// quadrant, each owning half of the keys and half of every output block), warps 4-7 gather the
 // selected rows with cp.async (eight threads per 128-byte row segment, so every warp instruction
-// moves four whole segments) into the 128-byte-swizzled operand layout, warp 8 issues tcgen05.mma.
+// moves four whole segments) into the 128-byte-swizzled operand layout, warp 12 issues
+// tcgen05.mma.
 //   A  S[128 heads x 512 keys] = Q K^T accumulates over 9 chunks of 64 dims: per chunk a Q
 //      chunk (tiled TMA) and the chunk of all 512 gathered key rows; 4 MMAs of N = 128 keys per
 //      16-dim step into TMEM columns 0..511.
@@ -59,12 +61,14 @@ constexpr int kRegion = kPBytes + 2 * kVStageBytes;  // 192 KB
 static_assert(2 * kAStageBytes <= kRegion, "phase A stages fit the shared region");
 constexpr int kOffRows = kRegion;                   // int32 gather rows [512]
 constexpr int kOffMask = kOffRows + kK * 4;         // uint32 validity words [16]
-constexpr int kOffBars = kOffMask + 64;
+constexpr int kOffRed = kOffMask + 64;              // float [2 halves][2][128]: max, sum
+constexpr int kOffBars = kOffRed + 2 * 2 * kH * 4;
 constexpr int kNumBars = 2 + 2 + 1 + 1 + 2 + 2 + 1;
 constexpr int kOffMisc = kOffBars + kNumBars * 8;
 constexpr int kSmemBytes = kOffMisc + 32 + 1024;
-constexpr int kProducer0 = 4, kProducers = 4, kMma = 8;
+constexpr int kProducer0 = 4, kProducers = 4, kSoftmax1 = 8, kMma = 12;
 constexpr int kThreads = (kMma + 1) * 32;
+constexpr int kSoftmaxThreads = 8 * 32;
 constexpr int kProducerThreads = kProducers * 32;
 // B operand of P.V: V chunk rows are keys (the K dimension), 64 value dims per 128-byte row
 // (the N dimension): an MN-major operand. Atoms of 8 keys x 64 dims (1 KB) repeat every 1 KB
@@ -94,11 +98,11 @@ __device__ __forceinline__ void gather4(void* dst, const CUtensorMap* m, uint64_
       : "memory");
 }
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uint64_t* bar,
-                                            int32_t x, int32_t y) {
+                                            int32_t x, int32_t y, uint64_t pol) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
       : "memory");
 }
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle layout.
@@ -112,8 +116,26 @@ __device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t 
   d |= static_cast<uint64_t>(2u) << 61;
   return d;
 }
-__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+// L2 policies: the latent rows are gathered many times (keep them), queries and outputs pass once.
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, uint64_t pol) {
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)),
+               "l"(src), "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void st_global_v4(void* dst, uint4 v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(dst), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
@@ -153,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(s_ready, 1);
-    mbar_init(p_ready, 4);
+    mbar_init(p_ready, 8);
     mbar_init(o_ready, 1);
     *s_abort = 0u;
     fence_mbar_init();
@@ -184,6 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pt = threadIdx.x - kProducer0 * 32;  // 0..127
     const int pw = pt >> 5;
     const int seg = lane & 7, sub = lane >> 3;      // K rows: 8 threads per 128-byte segment
+    const uint64_t keep = policy_evict_last(), pass = policy_evict_first();
     int issued_q = 0;
     bool ok = true;
     for (int c = 0; c < kNChunks; ++c) {
@@ -192,14 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* base = smem + st * kAStageBytes;
       if (pt == 0) {
         mbar_arrive_expect_tx(&a_full[st], kH * 128);
-        tma_load_2d(base, &tmap_q, &a_full[st], c * kChunk, static_cast<int32_t>(t * kH));
+        tma_load_2d(base, &tmap_q, &a_full[st], c * kChunk, static_cast<int32_t>(t * kH), pass);
         issued_q = c + 1;
       }
       uint8_t* kbase = base + kH * 128;
       for (int i = 0; i < kK / (4 * kProducers); ++i) {
         const int r = (i * kProducers + pw) * 4 + sub;  // key row 0..511
         cp_async16(kbase + r * 128 + ((seg ^ (r & 7)) * 16),
-                   kv + static_cast<int64_t>(s_rows[r]) * kDqk + c * kChunk + seg * 8);
+                   kv + static_cast<int64_t>(s_rows[r]) * kDqk + c * kChunk + seg * 8, keep);
       }
       cp_async_commit();
       if (c > 0) {
@@ -222,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int r = j * kProducers + pw;  // 0..63 within the chunk
           const int nb = lane >> 3, cc = lane & 7;
           cp_async16(base + nb * kVStrideN + r * 128 + ((cc ^ (r & 7)) * 16),
-                     kv + static_cast<int64_t>(s_rows[kc * kVKeys + r]) * kDqk + half * 256 + lane * 8);
+                     kv + static_cast<int64_t>(s_rows[kc * kVKeys + r]) * kDqk + half * 256 + lane * 8,
+                     keep);
         }
         cp_async_commit();
         if (i > 0) {
@@ -281,79 +305,101 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else {
-    // ---------------- softmax and output (thread = head)
-    const int h = warp * 32 + lane;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ---------------- softmax and output: lane quadrant warp % 4, key half g
+    const int g = warp >= kSoftmax1 ? 1 : 0;
+    const int quad = warp & 3;
+    const int h = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    float* red = reinterpret_cast<float*>(smem + kOffRed);  // [stat][g][h]
+    auto softmax_sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads) : "memory"); };
     float m = -__int_as_float(0x7f800000), l = 0.f;
     bool ok = mbar_wait_warp(s_ready, 0u, s_abort, err);
     tc_fence_after();
+    constexpr int kHalfChunks = kK / 32 / 2;  // 8 chunks of 32 keys per key half
+    const int i0 = g * kHalfChunks;
     if (ok) {
-      // Two passes over S, each reading 32-column chunks with the next chunk's load in flight.
+      // Two passes over this thread's half of S, each reading 32-column chunks with the next
+      // chunk's load in flight; the two halves combine their max and sum in shared memory.
       uint32_t rb[2][32];
-      tmem_ld32(tmem + lane_base, rb[0]);
+      tmem_ld32(tmem + lane_base + 32 * i0, rb[0]);
       tmem_wait_ld();
+      float mx = -__int_as_float(0x7f800000);
 #pragma unroll 2
-      for (int i = 0; i < kK / 32; ++i) {
-        if (i + 1 < kK / 32) tmem_ld32(tmem + lane_base + 32 * (i + 1), rb[(i + 1) & 1]);
+      for (int i = 0; i < kHalfChunks; ++i) {
+        if (i + 1 < kHalfChunks) tmem_ld32(tmem + lane_base + 32 * (i0 + i + 1), rb[(i + 1) & 1]);
         const uint32_t* r = rb[i & 1];
-        const uint32_t vm = s_mask[i];
+        const uint32_t vm = s_mask[i0 + i];
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-          if ((vm >> j) & 1u) m = fmaxf(m, __uint_as_float(r[j]) * p.scale_log2);
+          mx = fmaxf(mx, ((vm >> j) & 1u) ? __uint_as_float(r[j]) : -__int_as_float(0x7f800000));
         tmem_wait_ld();
       }
+      red[g * kH + h] = mx * p.scale_log2;  // scale > 0: the max of the scaled scores
+    }
+    softmax_sync();  // every softmax warp reaches it, also after an abort
+    if (ok) {
+      uint32_t rb[2][32];
+      m = fmaxf(red[h], red[kH + h]);
       const float mm = m == -__int_as_float(0x7f800000) ? 0.f : m;
-      tmem_ld32(tmem + lane_base, rb[0]);
+      tmem_ld32(tmem + lane_base + 32 * i0, rb[0]);
       tmem_wait_ld();
+      float ls = 0.f;
 #pragma unroll 2
-      for (int i = 0; i < kK / 32; ++i) {
-        if (i + 1 < kK / 32) tmem_ld32(tmem + lane_base + 32 * (i + 1), rb[(i + 1) & 1]);
+      for (int i = 0; i < kHalfChunks; ++i) {
+        if (i + 1 < kHalfChunks) tmem_ld32(tmem + lane_base + 32 * (i0 + i + 1), rb[(i + 1) & 1]);
         const uint32_t* r = rb[i & 1];
-        const uint32_t vm = s_mask[i];
+        const uint32_t vm = s_mask[i0 + i];
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           const float p0 = ((vm >> j) & 1u) ? exp2f(__uint_as_float(r[j]) * p.scale_log2 - mm) : 0.f;
           const float p1 = ((vm >> (j + 1)) & 1u) ? exp2f(__uint_as_float(r[j + 1]) * p.scale_log2 - mm) : 0.f;
-          l += p0 + p1;
+          ls += p0 + p1;
           pk[j / 2] = pack_bf16x2(p0, p1);
         }
-        // keys 32i..32i+31 of head h: block i/2, 16-byte chunks (i%2)*4 .. +3 of row h
-        uint8_t* row = smem + kOffP + (i >> 1) * (kH * 128) + h * 128;
+        // keys 32(i0+i)..+31 of head h: block (i0+i)/2, 16-byte chunks ((i0+i)%2)*4 .. +3 of row h
+        const int ci = i0 + i;
+        uint8_t* row = smem + kOffP + (ci >> 1) * (kH * 128) + h * 128;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int cc = (i & 1) * 4 + u;
+          const int cc = (ci & 1) * 4 + u;
           *reinterpret_cast<uint4*>(row + ((cc ^ (h & 7)) * 16)) =
               make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
         }
         tmem_wait_ld();
       }
+      red[2 * kH + g * kH + h] = ls;
     }
     fence_proxy_async_smem();  // P (generic writes) before the MMAs that read it
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(p_ready);
-    if (p.lse)
+    softmax_sync();  // both halves' sums are in shared memory
+    if (ok) l = red[2 * kH + h] + red[3 * kH + h];
+    if (p.lse && g == 0)
       p.lse[t * kH + h] = l > 0.f ? (m + __log2f(l)) * 0.69314718055994531f : -__int_as_float(0x7f800000);
     const float inv = l > 0.f ? 1.f / l : 0.f;
     uint16_t* orow = p.out + (t * kH + h) * kDv;
+    const uint64_t pass = policy_evict_first();
     for (int half = 0; ok && half < 2; ++half) {
       if (!(ok = mbar_wait_warp(o_ready, static_cast<uint32_t>(half), s_abort, err))) break;
       tc_fence_after();
+      // this warp stores value dims 256 half + 128 g .. + 127
       uint32_t rb[2][32];
-      const uint32_t ocol = tmem + lane_base + 256 * half;
+      const uint32_t ocol = tmem + lane_base + 256 * half + 128 * g;
       tmem_ld32(ocol, rb[0]);
       tmem_wait_ld();
-      for (int i = 0; i < 8; ++i) {
-        if (i + 1 < 8) tmem_ld32(ocol + 32 * (i + 1), rb[(i + 1) & 1]);
+      for (int i = 0; i < 4; ++i) {
+        if (i + 1 < 4) tmem_ld32(ocol + 32 * (i + 1), rb[(i + 1) & 1]);
         const uint32_t* r = rb[i & 1];
         uint32_t pk[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2)
           pk[j / 2] = pack_bf16x2(__uint_as_float(r[j]) * inv, __uint_as_float(r[j + 1]) * inv);
-        uint4* dst = reinterpret_cast<uint4*>(orow + half * 256 + 32 * i);
+        uint4* dst = reinterpret_cast<uint4*>(orow + half * 256 + 128 * g + 32 * i);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+        for (int u = 0; u < 4; ++u)
+          st_global_v4(dst + u, make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]), pass);
         tmem_wait_ld();
       }
     }
