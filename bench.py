@@ -701,7 +701,8 @@ def run_attention(args, rank, world, local_rank):
                            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
                 "roofline": {"bound": "tensor", "achieved": achieved,
                              "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                             "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                             "frac": achieved / peaks["bf16_tflops"],
+                             "traffic": traffic_for(args.workload),
                              "peak_source": f"bf16 dense, {peak_src} (burst)",
                              "algorithmic": f"{flops:.4g} flop = 2*128*(576+512) * {valid} "
                                             f"selected (token, key) pairs",
