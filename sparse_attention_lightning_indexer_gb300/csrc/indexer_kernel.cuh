@@ -398,7 +398,7 @@ template <int NT>
 __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, int n, uint32_t lo,
                            uint32_t hi, int warp, int lane) {
   constexpr int kWarps = NT / 32;
-  static_assert(kWarps + 1 <= 256, "per-warp sums fit the radix scratch");
+  static_assert(kWarps + 1 <= 256 && kWarps <= 32, "per-warp sums fit the radix scratch and a warp");
   int e = 0;
   while (e < 20 && ((static_cast<int>(hi - lo) + 1) << (e + 1)) <= kRankBins) ++e;
   const int range = (static_cast<int>(hi - lo) + 1) << e;
@@ -430,8 +430,7 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
   }
   if (lane == 31) ra.rhist[warp] = s;
   __syncthreads();
-  uint32_t run = s - own;
-  for (int w = 0; w < warp; ++w) run += ra.rhist[w];
+  uint32_t run = s - own + __reduce_add_sync(0xffffffffu, lane < warp ? ra.rhist[lane] : 0u);
   for (int v = v0; v < v0 + per && v < range; ++v) {
     const int r = range - 1 - v;
     ra.off[r] = run;
@@ -619,8 +618,10 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   constexpr int kCap = C::kStages * C::kKBytes / 8;  // words of the gather area
   constexpr int kHead = kSlotListOff;                // header + window words of a slot
   static_assert(64 * kHead <= kCap, "every split's header and window fit at once");
+  static_assert(kWarps <= 32, "one lane per warp in the slice scan");
   const RankArea ra(area);
-  uint32_t* mh = reinterpret_cast<uint32_t*>(ra.sv);  // kHBins counts, until sv is filled
+  uint32_t* mh = ra.cnt;      // summed window counts of bins top, top - 1, .. (cnt, off, cur)
+  static_assert(3 * kRankBins >= kHBins, "summed windows fit");
   uint32_t* hm = ra.hdr;      // [64] list sizes
   uint32_t* hlo = hm + 64;    // [64] window starts
   uint32_t* hnb = hlo + 64;   // [64] window widths
@@ -629,7 +630,6 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   const int ns = sd.n_splits;
   const int64_t row = sd.q_row0 + t0;
   const uint64_t* slots = p.partial + sd.list0 + t0 * ns * kSlotWords;
-  for (int i = threadIdx.x; i < kHBins; i += NT) mh[i] = 0u;
   fence_proxy_async_smem();  // earlier generic accesses to the copy targets precede the copies
   __syncthreads();
   if (warp == 0) {
@@ -654,33 +654,56 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
     hnb[i] = (nb <= static_cast<uint32_t>(kSlotHistBins) && lo + nb <= static_cast<uint32_t>(kHBins)) ? nb : 0u;
   }
   __syncthreads();
-  for (int j = threadIdx.x; j < ns * kSlotHistBins; j += NT) {
-    const int i = j / kSlotHistBins, k = j - i * kSlotHistBins;
-    if (k < static_cast<int>(hnb[i])) {
-      const uint32_t c = reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords)[k];
-      if (c) atomicAdd(&mh[hlo[i] + k], c);
+  // The counted range [bottom, top] (every warp finds it). Thread t sums the windows over its
+  // slice of `per` bins from the top down (no atomics); a CTA-wide scan of the slice totals
+  // then shows the slice, and the bin, where the count from the top first reaches 512.
+  uint32_t top = 0u, bottom = kHBins - 1;
+  for (int i = lane; i < ns; i += 32)
+    if (hnb[i]) {
+      top = max(top, hlo[i] + hnb[i] - 1u);
+      bottom = min(bottom, hlo[i]);
     }
+  top = __reduce_max_sync(0xffffffffu, top);
+  bottom = __reduce_min_sync(0xffffffffu, bottom);
+  bottom = bottom < top ? bottom : top;  // lowest counted bin (top itself when nothing counted)
+  const int per = (static_cast<int>(top - bottom) + NT) / NT;
+  const int r0 = static_cast<int>(threadIdx.x) * per;  // offsets below top: bins top - r
+  const int r1 = min(r0 + per, static_cast<int>(top - bottom) + 1);
+  uint32_t own = 0u;
+  for (int r = r0; r < r1; ++r) {
+    const uint32_t bin = top - static_cast<uint32_t>(r);
+    uint32_t c = 0u;
+    for (int i = 0; i < ns; ++i) {
+      const uint32_t k = bin - hlo[i];  // wraps above hnb when bin < hlo
+      if (k < hnb[i]) c += reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords)[k];
+    }
+    mh[r] = c;
+    own += c;
   }
-  if (warp == 0) {
-    uint32_t top = 0u, bottom = kHBins - 1;
-    for (int i = lane; i < ns; i += 32)
-      if (hnb[i]) {
-        top = max(top, hlo[i] + hnb[i] - 1u);
-        bottom = min(bottom, hlo[i]);
-      }
-    top = __reduce_max_sync(0xffffffffu, top);
-    bottom = __reduce_min_sync(0xffffffffu, bottom);
-    if (lane == 0) {
-      scratch[1] = top;
-      scratch[3] = bottom < top ? bottom : top;  // lowest counted bin
-    }
+  uint32_t incl = own;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  uint32_t* wsum = ra.rhist;  // [kWarps] slice totals per warp
+  if (lane == 31) wsum[warp] = incl;
+  if (threadIdx.x == 0) {
+    scratch[0] = 0u;  // G = 0 (every published word stays) unless some bin reaches 512
+    scratch[1] = top;
   }
   __syncthreads();
-  if (warp == 0) {
-    uint32_t c;
-    // Only counted bins can reach 512; when none does, every published word stays (G = 0).
-    const uint32_t g = warp_find_cut<kTopK>(Hist32{mh}, scratch[3], scratch[1], &c, lane);
-    if (lane == 0) scratch[0] = c >= static_cast<uint32_t>(kTopK) ? g : 0u;
+  const uint32_t above =
+      incl - own + __reduce_add_sync(0xffffffffu, lane < warp ? wsum[lane] : 0u);
+  if (above < static_cast<uint32_t>(kTopK) && above + own >= static_cast<uint32_t>(kTopK)) {
+    uint32_t run = above;  // exactly one thread crosses 512 inside its slice
+    for (int r = r0; r < r1; ++r) {
+      run += mh[r];
+      if (run >= static_cast<uint32_t>(kTopK)) {
+        scratch[0] = top - static_cast<uint32_t>(r);
+        break;
+      }
+    }
   }
   __syncthreads();
   const uint32_t G = scratch[0], H = scratch[1];
@@ -716,8 +739,7 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
     }
     if (lane == 0) hpre[ns] = acc;
   }
-  fence_proxy_async_smem();  // sv held the summed counts (generic accesses) before the copies
-  __syncthreads();
+  __syncthreads();  // sv took no generic accesses since the fence above: no second fence
   const int total = static_cast<int>(hpre[ns]);
   if (total <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins)) {
     if (warp == 0) {
