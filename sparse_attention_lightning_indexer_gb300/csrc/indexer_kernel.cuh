@@ -606,8 +606,9 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
 // histogram, whose scan gives the highest bin G that at least 512 published words reach (the
 // 512th best word overall lies in G or above). Each list is grouped by bin, so its words at or
 // above G are a prefix whose length its window gives (a whole list when G lies below its
-// window); a second round of bulk copies brings just those prefixes, and rank_write orders the
-// words with bin >= G. More of them than the ranking takes fall back to a radix select over all
+// window). The first round also brought each list's first words, which usually hold those
+// prefixes; otherwise a second round of bulk copies brings them. rank_write orders the words
+// with bin >= G. More of them than the ranking takes fall back to a radix select over all
 // lists and one CTA-wide sort.
 template <class C>
 __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0, uint64_t* buf,
@@ -617,7 +618,12 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   constexpr int kWarps = NT / 32;
   constexpr int kCap = C::kStages * C::kKBytes / 8;  // words of the gather area
   constexpr int kHead = kSlotListOff;                // header + window words of a slot
-  static_assert(64 * kHead <= kCap, "every split's header and window fit at once");
+  // The first round of copies also brings the first kPre words of each list: when every
+  // list's words at or above the cut are among them (the usual case), no second round is needed.
+  constexpr int kPre = 64;
+  constexpr int kRound1 = kHead + kPre;
+  static_assert(64 * kRound1 <= kCap && kRound1 <= kSlotWords && kRound1 % 2 == 0,
+                "every split's header, window and first words fit at once");
   static_assert(kWarps <= 32, "one lane per warp in the slice scan");
   const RankArea ra(area);
   uint32_t* mh = ra.cnt;      // summed window counts of bins top, top - 1, .. (cnt, off, cur)
@@ -633,11 +639,11 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   fence_proxy_async_smem();  // earlier generic accesses to the copy targets precede the copies
   __syncthreads();
   if (warp == 0) {
-    if (lane == 0) mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(ns * kHead * 8));
+    if (lane == 0) mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(ns * kRound1 * 8));
     __syncwarp();
     fence_proxy_async_global();  // the slots published by other CTAs, seen by the copies
     for (int i = lane; i < ns; i += 32)
-      bulk_load(buf + i * kHead, slots + static_cast<int64_t>(i) * kSlotWords, kHead * 8, gbar);
+      bulk_load(buf + i * kRound1, slots + static_cast<int64_t>(i) * kSlotWords, kRound1 * 8, gbar);
   }
   // CTA-uniform outcome: a thread may see the copies land while another gives up.
   if (!__syncthreads_and(mbar_wait(gbar, 0u, abort_flag, p.err, p.wait_ns))) {
@@ -645,7 +651,7 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
     return;
   }
   for (int i = threadIdx.x; i < ns; i += NT) {
-    const uint64_t h = buf[i * kHead];
+    const uint64_t h = buf[i * kRound1];
     const uint32_t m = static_cast<uint32_t>(h);
     const uint32_t lo = static_cast<uint32_t>(h >> 32) & 0xFFFFu;
     const uint32_t nb = static_cast<uint32_t>(h >> 48);
@@ -673,9 +679,10 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   for (int r = r0; r < r1; ++r) {
     const uint32_t bin = top - static_cast<uint32_t>(r);
     uint32_t c = 0u;
+#pragma unroll 4
     for (int i = 0; i < ns; ++i) {
       const uint32_t k = bin - hlo[i];  // wraps above hnb when bin < hlo
-      if (k < hnb[i]) c += reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords)[k];
+      if (k < hnb[i]) c += reinterpret_cast<const uint32_t*>(buf + i * kRound1 + kSlotHdrWords)[k];
     }
     mh[r] = c;
     own += c;
@@ -714,7 +721,7 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
     if (G <= hlo[i]) {
       n = hm[i];
     } else {
-      const uint32_t* win = reinterpret_cast<const uint32_t*>(buf + i * kHead + kSlotHdrWords);
+      const uint32_t* win = reinterpret_cast<const uint32_t*>(buf + i * kRound1 + kSlotHdrWords);
       uint32_t s = 0u;
       for (int k = static_cast<int>(G - hlo[i]) + lane; k < static_cast<int>(hnb[i]); k += 32) s += win[k];
       n = __reduce_add_sync(0xffffffffu, s);
@@ -725,8 +732,10 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
   __syncthreads();
   if (warp == 0) {
     uint32_t acc = 0u;
+    bool fits = true;  // every list's words at or above G came with the first round
     for (int i0 = 0; i0 < ns; i0 += 32) {
       const int i = i0 + lane;
+      fits = __all_sync(0xffffffffu, i >= ns || hn[i] <= static_cast<uint32_t>(kPre)) && fits;
       const uint32_t sz = i < ns ? (hn[i] + 1u) & ~1u : 0u;
       uint32_t s = sz;
 #pragma unroll
@@ -737,10 +746,23 @@ __device__ void merge_hist_slots(const KParams& p, const SeqDesc& sd, int64_t t0
       if (i < ns) hpre[i] = acc + s - sz;
       acc += __shfl_sync(0xffffffffu, s, 31);
     }
-    if (lane == 0) hpre[ns] = acc;
+    if (lane == 0) {
+      hpre[ns] = acc;
+      scratch[2] = fits ? 1u : 0u;
+    }
   }
   __syncthreads();  // sv took no generic accesses since the fence above: no second fence
   const int total = static_cast<int>(hpre[ns]);
+  if (total <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins) && scratch[2]) {
+    for (int i = warp; i < ns; i += kWarps) {  // the prefixes, from the first round's copies
+      const uint64_t* src = buf + i * kRound1 + kHead;
+      const uint32_t n = hn[i], sz = (n + 1u) & ~1u;
+      for (uint32_t k = lane; k < sz; k += 32) ra.sv[hpre[i] + k] = k < n ? src[k] : 0ull;
+    }
+    __syncthreads();
+    rank_write<NT>(p, row, ra, total, G, H, warp, lane);
+    return;
+  }
   if (total <= kSurvCap && H - G < static_cast<uint32_t>(kRankBins)) {
     if (warp == 0) {
       if (lane == 0) mbar_arrive_expect_tx(gbar, static_cast<uint32_t>(total) * 8u);
