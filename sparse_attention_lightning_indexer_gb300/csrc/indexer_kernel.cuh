@@ -387,9 +387,9 @@ __device__ void finish_cta_select(const KParams& p, const SeqDesc& sd, int64_t t
   if (sd.n_splits > 1) fence_proxy_async_global();
 }
 
-// Writes the (up to) 512 best of the distinct words in ra.sv[0..n) whose bins lie in [lo, hi]
-// (others, such as zero padding, are skipped) as output row `row`, best first; hi - lo <
-// kRankBins. Words are bucketed by their bin refined with e more bits of the code (e as large
+// Writes the (up to) 512 best of the distinct words in ra.sv[0..n) (n <= kSurvCap) whose bins
+// lie in [lo, hi] (others, such as zero padding, are skipped) as output row `row`, best first;
+// hi - lo < kRankBins. Words are bucketed by their bin refined with e more bits of the code (e as large
 // as kRankBins buckets allow); a counting sort over the buckets (best first, CTA-wide suffix
 // scan) gives each bucket its range of positions, and a word's final position is its bucket's
 // first position plus the number of larger words in the same bucket (buckets hold a few words).
@@ -411,9 +411,18 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
   auto bucket = [&](uint64_t u) { return static_cast<int>((u >> shift) - base); };
   for (int i = threadIdx.x; i < range; i += NT) ra.cnt[i] = 0u;
   __syncthreads();
-  for (int i = threadIdx.x; i < n; i += NT) {
-    const uint64_t u = ra.sv[i];
-    if (in_range(u)) atomicAdd(&ra.cnt[bucket(u)], 1u);
+  // Counting also hands each word its slot within its bucket (kept in registers for the
+  // scatter below).
+  constexpr int kIter = (kSurvCap + NT - 1) / NT;
+  uint32_t slot_in[kIter];
+#pragma unroll
+  for (int j = 0; j < kIter; ++j) {
+    const int i = static_cast<int>(threadIdx.x) + j * NT;
+    slot_in[j] = 0u;
+    if (i < n) {
+      const uint64_t u = ra.sv[i];
+      if (in_range(u)) slot_in[j] = atomicAdd(&ra.cnt[bucket(u)], 1u);
+    }
   }
   __syncthreads();
   // off[r] = words in buckets above r. Thread t owns the buckets v = t*per .. t*per+per-1 counted
@@ -434,15 +443,18 @@ __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, in
   for (int v = v0; v < v0 + per && v < range; ++v) {
     const int r = range - 1 - v;
     ra.off[r] = run;
-    ra.cur[r] = run;
     run += ra.cnt[r];
   }
   if (threadIdx.x == NT - 1) ra.rhist[kWarps] = run;  // words in range
   __syncthreads();
   const int nv = static_cast<int>(ra.rhist[kWarps]);
-  for (int i = threadIdx.x; i < n; i += NT) {
-    const uint64_t u = ra.sv[i];
-    if (in_range(u)) ra.sorted[atomicAdd(&ra.cur[bucket(u)], 1u)] = u;
+#pragma unroll
+  for (int j = 0; j < kIter; ++j) {
+    const int i = static_cast<int>(threadIdx.x) + j * NT;
+    if (i < n) {
+      const uint64_t u = ra.sv[i];
+      if (in_range(u)) ra.sorted[ra.off[bucket(u)] + slot_in[j]] = u;
+    }
   }
   __syncthreads();
   int32_t* oi = p.out_idx + row * kTopK;
@@ -496,6 +508,18 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
   constexpr int kWarps = NT / 32;
   constexpr int kSegs = C::kEpiWarps;
   const int64_t row = sd.q_row0 + t0;
+  bool listed = true;
+#pragma unroll
+  for (int s = 0; s < kSegs; ++s) listed = listed && ncand[s] <= static_cast<uint32_t>(C::kCandSeg);
+  const bool split_plan = sd.n_splits > 1;
+  RankArea ra(reinterpret_cast<uint8_t*>(stage));
+  // The bucket window of a published slot (from the top bin down; see below).
+  auto slot_window = [&](uint32_t bs, int mm, uint32_t* wlo_out) -> int {
+    const uint32_t wlo = maxbin - bs >= static_cast<uint32_t>(kSlotHistBins)
+                             ? maxbin - (kSlotHistBins - 1) : bs;
+    *wlo_out = wlo;
+    return mm > 0 ? static_cast<int>(maxbin - wlo) + 1 : 0;
+  };
   if (warp == 0) {
     uint32_t m;
     const uint32_t bs =
@@ -504,17 +528,18 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
       scratch[0] = bs;
       scratch[1] = m;
     }
+    if (split_plan && listed && m <= static_cast<uint32_t>(kSlotListCap)) {
+      // the slot's bucket starts right away (the fast split path below uses them)
+      uint32_t wlo;
+      const int nb = slot_window(bs, static_cast<int>(m), &wlo);
+      slot_bucket_starts(Hist16{bins}, maxbin, nb, ra.cur, lane);
+    }
   }
   __syncthreads();
   const uint32_t bstar = scratch[0];
   const int m = static_cast<int>(scratch[1]);
-  bool listed = true;
-#pragma unroll
-  for (int s = 0; s < kSegs; ++s) listed = listed && ncand[s] <= static_cast<uint32_t>(C::kCandSeg);
-  const bool split_plan = sd.n_splits > 1;
   uint64_t* slot =
       split_plan ? p.partial + sd.list0 + (t0 * sd.n_splits + split) * kSlotWords : nullptr;
-  RankArea ra(reinterpret_cast<uint8_t*>(stage));
   const bool fast = listed && (split_plan ? m <= kSlotListCap
                                           : (m <= kSurvCap && maxbin - bstar < kRankBins));
   if (fast) {
@@ -529,15 +554,25 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
     };
     if (split_plan) {
       // Grouped by bin (window bins from the top, then the rest) straight into the slot.
-      const uint32_t wlo = maxbin - bstar >= static_cast<uint32_t>(kSlotHistBins)
-                               ? maxbin - (kSlotHistBins - 1) : bstar;
-      const int nb = m > 0 ? static_cast<int>(maxbin - wlo) + 1 : 0;
-      if (warp == 0) slot_bucket_starts(Hist16{bins}, maxbin, nb, ra.cur, lane);
-      __syncthreads();
+      uint32_t wlo;
+      const int nb = slot_window(bstar, m, &wlo);  // (bucket starts: set before the barrier)
       uint64_t* dst = slot + kSlotListOff;
-#pragma unroll 2
-      for (int i = threadIdx.x; i < kSpan; i += NT) {
-        const uint64_t u = word_at(i);
+      // Only the listed entries: the lists' lengths, flattened (list s starts at seg[s]).
+      uint32_t seg[kSegs + 1];
+      seg[0] = 0u;
+#pragma unroll
+      for (int j = 0; j < kSegs; ++j)
+        seg[j + 1] = seg[j] + min(ncand[j], static_cast<uint32_t>(C::kCandSeg));
+      for (int x = threadIdx.x; x < static_cast<int>(seg[kSegs]); x += NT) {
+        int sx = 0;
+        uint32_t base = 0u;
+#pragma unroll
+        for (int j = 1; j < kSegs; ++j)
+          if (static_cast<uint32_t>(x) >= seg[j]) {
+            sx = j;
+            base = seg[j];
+          }
+        const uint64_t u = word_at(sx * C::kCandSeg + (x - static_cast<int>(base)));
         if (u) {
           const uint32_t bn = hbin(u);
           const int r = bn >= wlo ? static_cast<int>(maxbin - bn) : nb;
