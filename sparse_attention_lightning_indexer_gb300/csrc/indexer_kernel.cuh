@@ -206,8 +206,10 @@ struct KCfg {
   // the ring and the pools, which that mode leaves unused, plus whatever shared memory is left.
   static constexpr bool kHistSel = NQ == 1 && !DENSE;
   static constexpr int kBinsBytes = kHBins * 2 + (kHBins / 32) * 4;  // bins, then 32-bin groups
-  static constexpr int kCandSeg = 512;  // candidate offsets per epilogue warp (16-bit)
-  static constexpr int kCandBytes = kHistSel ? kEpiWarps * kCandSeg * 2 : 0;
+  // Candidates per epilogue warp: each entry holds the key's offset in the split (low 16 bits)
+  // and its bin (high 16 bits), so the final filter by the exact cut reads nothing else.
+  static constexpr int kCandSeg = 512;
+  static constexpr int kCandBytes = kHistSel ? kEpiWarps * kCandSeg * 4 : 0;
   static constexpr int kBufTiles =
       kHistSel ? (232448 - 1024 - kMiscBytes - kNumBars * 8 - kOffHist - kBinsBytes - kCandBytes) /
                      (kTileKeys * 4)
@@ -500,7 +502,7 @@ struct ScoreWords {
 // ties, a very flat score distribution), fall back to a radix select over all buffered scores.
 template <class C>
 __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int split, uint32_t* bins,
-                            const uint16_t* cand, const uint32_t* ncand, const float* sbuf,
+                            const uint32_t* cand, const uint32_t* ncand, const float* sbuf,
                             int n_tiles, int64_t key0, int64_t vis_end, uint32_t floor_bin,
                             uint32_t maxbin, uint64_t* stage, uint32_t* scratch, int warp,
                             int lane) {
@@ -542,43 +544,48 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
       split_plan ? p.partial + sd.list0 + (t0 * sd.n_splits + split) * kSlotWords : nullptr;
   const bool fast = listed && (split_plan ? m <= kSlotListCap
                                           : (m <= kSurvCap && maxbin - bstar < kRankBins));
+  // A list entry's word, or 0 when its bin lies below the exact cut.
+  auto listed_word = [&](uint32_t e) -> uint64_t {
+    if ((e >> 16) < bstar) return 0ull;
+    const int k = static_cast<int>(e & 0xFFFFu);
+    return pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
+  };
   if (fast) {
     // The lists side by side: position i is entry i % kCandSeg of list i / kCandSeg.
     constexpr int kSpan = kSegs * C::kCandSeg;
     auto word_at = [&](int i) -> uint64_t {
       const int s = i / C::kCandSeg;
       if (static_cast<uint32_t>(i - s * C::kCandSeg) >= ncand[s]) return 0ull;
-      const int k = cand[i];
-      const uint64_t u = pack_key(sbuf[k], static_cast<uint32_t>(key0 + k));
-      return hbin(u) >= bstar ? u : 0ull;
+      return listed_word(cand[i]);
     };
     if (split_plan) {
       // Grouped by bin (window bins from the top, then the rest) straight into the slot.
       uint32_t wlo;
       const int nb = slot_window(bstar, m, &wlo);  // (bucket starts: set before the barrier)
       uint64_t* dst = slot + kSlotListOff;
-      // Only the listed entries: the lists' lengths, flattened (list s starts at seg[s]).
-      uint32_t seg[kSegs + 1];
-      seg[0] = 0u;
+      // Thread t takes entry t (then t + NT) of every list: the lists' candidates are read and
+      // filtered first, then all of a thread's slot claims (shared-memory atomics) are made
+      // before any is used, then the words are stored.
+      uint32_t nc[kSegs];
 #pragma unroll
-      for (int j = 0; j < kSegs; ++j)
-        seg[j + 1] = seg[j] + min(ncand[j], static_cast<uint32_t>(C::kCandSeg));
-      for (int x = threadIdx.x; x < static_cast<int>(seg[kSegs]); x += NT) {
-        int sx = 0;
-        uint32_t base = 0u;
+      for (int j = 0; j < kSegs; ++j) nc[j] = min(ncand[j], static_cast<uint32_t>(C::kCandSeg));
+      for (int e = threadIdx.x; e < C::kCandSeg; e += NT) {
+        uint64_t u[kSegs];
+        uint32_t pos[kSegs];
 #pragma unroll
-        for (int j = 1; j < kSegs; ++j)
-          if (static_cast<uint32_t>(x) >= seg[j]) {
-            sx = j;
-            base = seg[j];
+        for (int j = 0; j < kSegs; ++j)
+          u[j] = static_cast<uint32_t>(e) < nc[j] ? listed_word(cand[j * C::kCandSeg + e]) : 0ull;
+#pragma unroll
+        for (int j = 0; j < kSegs; ++j) {
+          pos[j] = 0u;
+          if (u[j]) {
+            const uint32_t bn = hbin(u[j]);
+            pos[j] = atomicAdd(&ra.cur[bn >= wlo ? static_cast<int>(maxbin - bn) : nb], 1u);
           }
-        const uint64_t u = word_at(sx * C::kCandSeg + (x - static_cast<int>(base)));
-        if (u) {
-          const uint32_t bn = hbin(u);
-          const int r = bn >= wlo ? static_cast<int>(maxbin - bn) : nb;
-          const uint32_t pos = atomicAdd(&ra.cur[r], 1u);
-          if (pos < static_cast<uint32_t>(kSlotListCap)) dst[pos] = u;  // never reached: m fit
         }
+#pragma unroll
+        for (int j = 0; j < kSegs; ++j)
+          if (u[j] && pos[j] < static_cast<uint32_t>(kSlotListCap)) dst[pos[j]] = u[j];  // m fits
       }
       uint32_t* sh = reinterpret_cast<uint32_t*>(slot + kSlotHdrWords);
       for (int i = threadIdx.x; i < nb; i += NT) sh[i] = Hist16{bins}(wlo + i);
@@ -911,7 +918,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   float* sScore = reinterpret_cast<float*>(smem + C::kOffRing);
   // buffered mode only: scores, candidate offsets, per-bin counts
   float* sBuf = reinterpret_cast<float*>(smem + C::kOffBuf);
-  uint16_t* s_cand = reinterpret_cast<uint16_t*>(smem + C::kOffCand);
+  uint32_t* s_cand = reinterpret_cast<uint32_t*>(smem + C::kOffCand);
   uint32_t* s_bins = reinterpret_cast<uint32_t*>(smem + C::kOffBins);
   uint32_t* s_grp = s_bins + kHBins / 2;  // 32-bin group counts
   uint64_t* sPool = reinterpret_cast<uint64_t*>(smem + C::kOffPool);
@@ -1135,7 +1142,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
       for (int i = 0; i < C::kQPerGroup * kHeads; ++i) wr[i] = sW[q0 * kHeads + i];
     }
     uint32_t own_cand = 0u;                                  // buffered mode: keys listed
-    uint16_t* own_list = s_cand + warp * C::kCandSeg;        // buffered mode: their offsets
+    uint32_t* own_list = s_cand + warp * C::kCandSeg;        // buffered mode: offsets and bins
     if (DT == kDtFp8) {
       ks_next0 = load_scale(it0);
       ks_next1 = load_scale(it0 + step);
@@ -1236,7 +1243,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                 hist16_inc(s_bins, bn);
                 atomicAdd(&s_grp[bn >> 5], 1u);
                 const uint32_t pos = own_cand + __popc(km & ((1u << lane) - 1u));
-                if (pos < static_cast<uint32_t>(C::kCandSeg)) own_list[pos] = static_cast<uint16_t>(k);
+                if (pos < static_cast<uint32_t>(C::kCandSeg))
+                  own_list[pos] = static_cast<uint32_t>(k) | (bn << 16);
               }
               const uint32_t before = own_cand;
               own_cand += static_cast<uint32_t>(__popc(km));
