@@ -201,9 +201,10 @@ struct KCfg {
   static constexpr uint32_t kWaitHint = NQ == 1 ? 20000u : 0u;
   // Buffered selection (one-query CTAs whose key split fits): the epilogue keeps every fp32
   // score of the split, counts the keys that reach a running cut bin per bin (16-bit counters)
-  // and lists their offsets (one list per epilogue warp), while a selector warp raises the cut;
-  // the final selection reads them back (finish_hist). These overlay the selector histograms,
-  // the ring and the pools, which that mode leaves unused, plus whatever shared memory is left.
+  // and lists their offsets and bins (one list per epilogue warp), while a selector warp raises
+  // the cut; the final selection reads them back (finish_hist). These overlay the selector
+  // histograms, the ring and the pools, which that mode leaves unused, plus whatever shared
+  // memory is left.
   static constexpr bool kHistSel = NQ == 1 && !DENSE;
   static constexpr int kBinsBytes = kHBins * 2 + (kHBins / 32) * 4;  // bins, then 32-bin groups
   // Candidates per epilogue warp: each entry holds the key's offset in the split (low 16 bits)
@@ -389,18 +390,19 @@ __device__ void finish_cta_select(const KParams& p, const SeqDesc& sd, int64_t t
   if (sd.n_splits > 1) fence_proxy_async_global();
 }
 
-// Writes the (up to) 512 best of the distinct words in ra.sv[0..n) (n <= kSurvCap) whose bins
-// lie in [lo, hi] (others, such as zero padding, are skipped) as output row `row`, best first;
-// hi - lo < kRankBins. Words are bucketed by their bin refined with e more bits of the code (e as large
-// as kRankBins buckets allow); a counting sort over the buckets (best first, CTA-wide suffix
-// scan) gives each bucket its range of positions, and a word's final position is its bucket's
-// first position plus the number of larger words in the same bucket (buckets hold a few words).
-// Buckets that start at or after position 512 are not ranked.
+// Writes the (up to) 512 best of the distinct words in ra.sv[0..n) (n <= kSurvCap) whose bins lie
+// in [lo, hi] (others, such as zero padding, are skipped) as output row `row`, best first; hi - lo
+// < kRankBins. Words are bucketed by their bin refined with e more bits of the code (e as large as
+// kRankBins buckets allow); a counting sort over the buckets (best first, CTA-wide suffix scan)
+// gives each bucket its range of positions, and a word's final position is its bucket's first
+// position plus the number of larger words in the same bucket (buckets hold a few words). Buckets
+// that start at or after position 512 are not ranked.
 template <int NT>
 __device__ void rank_write(const KParams& p, int64_t row, const RankArea& ra, int n, uint32_t lo,
                            uint32_t hi, int warp, int lane) {
   constexpr int kWarps = NT / 32;
-  static_assert(kWarps + 1 <= 256 && kWarps <= 32, "per-warp sums fit the radix scratch and a warp");
+  static_assert(kWarps + 1 <= 256 && kWarps <= 32,
+                "per-warp sums fit the radix scratch and one warp");
   int e = 0;
   while (e < 20 && ((static_cast<int>(hi - lo) + 1) << (e + 1)) <= kRankBins) ++e;
   const int range = (static_cast<int>(hi - lo) + 1) << e;
@@ -492,14 +494,14 @@ struct ScoreWords {
   }
 };
 
-// Finish of a one-query CTA in buffered mode. During the stream the epilogue kept each key's
-// fp32 score (sbuf) and listed, per epilogue warp, the offsets of the keys whose bin reached
-// the running cut bin at the time (cand, ncand) and counted them per bin (bins). Counts
-// at or above the final running cut are exact, so one scan finds the exact bin b* of the 512th
-// best word, and the listed keys with bin >= b* (at least 512 of them unless fewer are visible,
-// the CTA's 512 best among them) are read back. A split publishes them with its count window;
-// otherwise they are ranked and written. A full candidate list, or too many keys at b* (exact
-// ties, a very flat score distribution), fall back to a radix select over all buffered scores.
+// Finish of a one-query CTA in buffered mode. During the stream the epilogue kept each key's fp32
+// score (sbuf) and listed, per epilogue warp, the offsets and bins of the keys whose bin reached
+// the running cut bin at the time (cand, ncand) and counted them per bin (bins). Counts at or above
+// the final running cut are exact, so one scan finds the exact bin b* of the 512th best word, and
+// the listed keys with bin >= b* (at least 512 of them unless fewer are visible, the CTA's 512 best
+// among them) are read back. A split publishes them with its count window; otherwise they are
+// ranked and written. A full candidate list, or too many keys at b* (exact ties, a very flat score
+// distribution), fall back to a radix select over all buffered scores.
 template <class C>
 __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int split, uint32_t* bins,
                             const uint32_t* cand, const uint32_t* ncand, const float* sbuf,
