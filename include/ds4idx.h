@@ -178,7 +178,8 @@ uint64_t ds4idx_kernels_launched(void);
  * __device__ storage. Every GPU that loads the library holds that array until the process exits.
  *  - dtype is a ds4idx_dtype. All other arguments, layouts and rules are those of
  *    ds4idx_score_topk_batched, with 1 <= B <= 64, 0 <= T, 1 <= S < 2^31 and topk = 512.
- *  - Limit: the array holds 2^21 list words (16 MiB) and the split tickets of 4096 query blocks.
+ *  - Limit: the array holds 2^21 list words (16 MiB) and the split counters (merge ticket and
+ *    the splits' published bins) of 4096 query blocks.
  *    Short sequences (decode, small chunks) split their key range over several CTAs, and each
  *    split publishes a list of 512 words per query (1152 per one-query sequence). Here the split
  *    count steps down from the one ds4idx_score_topk_batched would use until the lists fit
@@ -189,10 +190,11 @@ uint64_t ds4idx_kernels_launched(void);
  *    attributes, with that device current. Make that first call before any stream capture.
  *  - Argument errors return INVALID_ARG before anything is enqueued or the array is touched.
  *  - Sharing: all calls use the same array, and it keeps the previous call's contents. The error
- *    word and the split tickets are cleared on `stream` at the start of every valid call; the
- *    candidate lists are always fully written before they are read. Calls that can overlap on the GPU (different streams or host
- *    threads without ordering between them) race on the array and corrupt each other's outputs,
- *    so order them, for example on one stream.
+ *    word and the split counters the call uses are cleared on `stream` at the start of every
+ *    valid call; the candidate lists are always fully written before they are read. Calls that
+ *    can overlap on the GPU (different streams or host threads without ordering between them)
+ *    race on the array and corrupt each other's outputs, so order them, for example on one
+ *    stream.
  *  - A kernel that gives up on a bounded device wait records it in the array's error word. This
  *    entry point cannot report it; callers that need that status use a handle and
  *    ds4idx_sync_status. */

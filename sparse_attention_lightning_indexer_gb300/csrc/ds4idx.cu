@@ -33,8 +33,8 @@ struct ds4idx_handle {
   uint32_t* err = nullptr;        // device error word
   uint64_t* partial = nullptr;    // per-split Top-512 lists
   size_t partial_words = 0;
-  uint32_t* counters = nullptr;   // per-block split tickets, zero between calls
-  size_t n_counters = 0;
+  uint32_t* counters = nullptr;   // per split query block: ticket and published bins, zero between calls
+  size_t n_counters = 0;          // split query blocks the counters hold
   uint64_t wait_ns = 0;           // bounded-wait limit passed to the kernels
   int32_t withhold = 0;           // test hook (ds4idx_debug_wait_test)
 };
@@ -42,8 +42,8 @@ struct ds4idx_handle {
 namespace {
 
 constexpr int kVersion = (1 << 16) | 1;
-// Fixed scratch of the no-allocation entry point: 2^21 list words (16 MiB) and the split
-// tickets of up to 4096 query blocks.
+// Fixed scratch of the no-allocation entry point: 2^21 list words (16 MiB) and the counters
+// (ticket and published bins) of up to 4096 split query blocks.
 constexpr size_t kNoAllocListWords = static_cast<size_t>(1) << 21;
 constexpr size_t kNoAllocTickets = 4096;
 constexpr int kMaxSplits = 64;
@@ -245,6 +245,7 @@ struct Call {
   KParams kp;
   bool dense = false;
   bool noop = false;  // no query at all
+  int64_t n_blocks = 0;  // split query blocks (counters) the call uses
 };
 
 // One sequence of a call, as the caller describes it.
@@ -429,6 +430,7 @@ int prepare(const Ctx& c, const CallSpec& cs, Call* call) {
     }
     ctas += static_cast<int64_t>(n_qb[b]) * n_splits[b];
   }
+  call->n_blocks = tickets;
   if (static_cast<size_t>(list) > c.partial_words || static_cast<size_t>(tickets) > c.n_counters)
     return c.cap_splits ? DS4IDX_ERR_SCRATCH_LIMIT : DS4IDX_ERR_INVALID_ARG;
   if (ctas > 0x7FFFFFFF) return DS4IDX_ERR_INVALID_ARG;
@@ -582,8 +584,9 @@ int ds4idx_create(ds4idx_t* out, const ds4idx_config* cfg) {
   }
   h->partial_words = words;
   h->n_counters = counters;
-  // err word at [0], split tickets from [64] (own cache lines), all zeroed once here
-  const size_t misc_bytes = 256 + counters * sizeof(uint32_t);
+  // err word at [0], split counters (ticket, published bins) from [64] (own cache lines), all
+  // zeroed once here
+  const size_t misc_bytes = 256 + counters * kCounterWords * sizeof(uint32_t);
   if (cudaMalloc(&h->err, misc_bytes) != cudaSuccess) {
     delete h;
     return DS4IDX_ERR_ALLOC;
@@ -677,7 +680,7 @@ int ds4idx_sync_status(ds4idx_t h, void* stream) {
     return DS4IDX_ERR_CUDA;
   if (word) {
     // A CTA that gave up may have left a split ticket half counted: start the next call clean.
-    cudaMemset(h->err, 0, 256 + h->n_counters * sizeof(uint32_t));
+    cudaMemset(h->err, 0, 256 + h->n_counters * kCounterWords * sizeof(uint32_t));
     return DS4IDX_ERR_DEVICE_TIMEOUT;
   }
   return DS4IDX_OK;
@@ -730,9 +733,10 @@ int ds4idx_destroy(ds4idx_t h) {
 namespace {
 
 // [0, kNoAllocListWords): per-split candidate lists; then the error word (own 256-byte line);
-// then the split tickets (32-bit, zeroed at every call together with the error word).
+// then the split counters (per split query block a ticket and the splits' published bins,
+// 32-bit; the blocks a call uses are zeroed at its start together with the error word).
 static __device__ __align__(256) uint64_t
-    g_noalloc_scratch[kNoAllocListWords + 32 + kNoAllocTickets / 2];
+    g_noalloc_scratch[kNoAllocListWords + 32 + kNoAllocTickets * kCounterWords / 2];
 
 struct NoAllocDevice {
   std::once_flag once;
@@ -821,8 +825,8 @@ extern "C" int ds4idx_score_topk_batched_noalloc(int32_t dtype, int32_t B, const
   if (vs != DS4IDX_OK) return vs;
   // Valid call: the array keeps the previous call's contents, so clear the error word and the
   // tickets on the stream right before the launch.
-  if (cudaMemsetAsync(c.err, 0, 256 + kNoAllocTickets * sizeof(uint32_t),
-                      static_cast<cudaStream_t>(stream)) != cudaSuccess)
+  const size_t clear = 256 + static_cast<size_t>(call.n_blocks) * kCounterWords * sizeof(uint32_t);
+  if (cudaMemsetAsync(c.err, 0, clear, static_cast<cudaStream_t>(stream)) != cudaSuccess)
     return DS4IDX_ERR_LAUNCH;
   return enqueue(c, call, stream);
 }

@@ -99,8 +99,7 @@ __device__ __forceinline__ uint32_t warp_find_cut(const Get get, uint32_t lo, ui
 // counts the words of bins 32g..32g+31): the groups above lo's group locate the cut's group,
 // whose bins are then read one by one, so the cost does not grow with the range. Groups are
 // only trusted above lo's group (their bins are all >= lo); lo's own group is read bin by bin.
-template <int K>
-__device__ __forceinline__ uint32_t warp_find_cut_grouped(const uint32_t* bins16,
+__device__ __forceinline__ uint32_t warp_find_cut_grouped(uint32_t K, const uint32_t* bins16,
                                                           const uint32_t* grp, uint32_t lo,
                                                           uint32_t hi, uint32_t* count, int lane) {
   const int glo = static_cast<int>(lo >> 5), ghi = static_cast<int>(hi >> 5);
@@ -115,7 +114,7 @@ __device__ __forceinline__ uint32_t warp_find_cut_grouped(const uint32_t* bins16
       if (lane >= off) s += v;
     }
     const uint32_t before = __shfl_up_sync(0xffffffffu, s, 1);
-    const uint32_t hit = __ballot_sync(0xffffffffu, acc + s >= static_cast<uint32_t>(K));
+    const uint32_t hit = __ballot_sync(0xffffffffu, acc + s >= K);
     if (hit) {
       const int l = __ffs(hit) - 1;
       acc += __shfl_sync(0xffffffffu, lane == 0 ? 0u : before, l);
@@ -133,7 +132,7 @@ __device__ __forceinline__ uint32_t warp_find_cut_grouped(const uint32_t* bins16
     const uint32_t v = __shfl_up_sync(0xffffffffu, s, off);
     if (lane >= off) s += v;
   }
-  const uint32_t hit = __ballot_sync(0xffffffffu, acc + s >= static_cast<uint32_t>(K));
+  const uint32_t hit = __ballot_sync(0xffffffffu, acc + s >= K);
   if (hit) {
     const int l = __ffs(hit) - 1;
     *count = acc + __shfl_sync(0xffffffffu, s, l);

@@ -62,6 +62,10 @@ constexpr int kSlotHdrWords = 2;
 constexpr int kSlotHistBins = 256;
 constexpr int kSlotListOff = kSlotHdrWords + kSlotHistBins / 2;
 constexpr int kSlotWords = 1152;
+// Per split query block in `counters`: its merge ticket, then one word per split (up to 64) in
+// which one-query splits publish a bin their k-th best key reaches, k = ceil(512 / splits). All
+// zero between calls (the merging CTA clears its block's words).
+constexpr int kCounterWords = 1 + 64;
 constexpr int kSlotListCap = kSlotWords - kSlotListOff;
 constexpr int kSurvCap = 2048;   // words the bin-ranked final selection takes at most
 constexpr int kRankBins = 2048;  // bins (and refined buckets) it spans at most
@@ -527,7 +531,7 @@ __device__ void finish_hist(const KParams& p, const SeqDesc& sd, int64_t t0, int
   if (warp == 0) {
     uint32_t m;
     const uint32_t bs =
-        warp_find_cut_grouped<kTopK>(bins, bins + kHBins / 2, floor_bin, maxbin, &m, lane);
+        warp_find_cut_grouped(kTopK, bins, bins + kHBins / 2, floor_bin, maxbin, &m, lane);
     if (lane == 0) {
       scratch[0] = bs;
       scratch[1] = m;
@@ -949,6 +953,8 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   uint32_t* s_ncand = reinterpret_cast<uint32_t*>(smem + C::kOffMisc + 104);  // [kEpiWarps]
   // The cut as a score threshold (bin_floor_score of the cut bin, or lower while it catches up).
   float* s_cutf = reinterpret_cast<float*>(smem + C::kOffMisc + 136);
+  // Set by the TMA producer once it has issued its last tile (the shared-cut loop stops).
+  volatile uint32_t* s_stream_done = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 140);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1012,6 +1018,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     *s_cut = 0u;
     *s_cutf = bin_floor_score(0u);
     *s_maxbin = 0u;
+    *s_stream_done = 0u;
     fence_mbar_init();
   }
   if (buffered)
@@ -1079,6 +1086,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
         mbar_drain(&full[j % C::kStages], (j / C::kStages) & 1);
       mbar_drain(qfull, 0);
     }
+    if (lane == 0) *s_stream_done = 1u;  // (also when this CTA had no tile to stream)
   };
   auto mma_role = [&]() {
     // ================= MMA issuer (one thread)
@@ -1262,7 +1270,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
                 lo = __shfl_sync(0xffffffffu, lo, 0);
                 hi = __shfl_sync(0xffffffffu, hi, 0);
                 const uint32_t nb =
-                    warp_find_cut_grouped<kTopK>(s_bins, s_grp, lo, hi >= lo ? hi : lo, &cnt, lane);
+                    warp_find_cut_grouped(kTopK, s_bins, s_grp, lo, hi >= lo ? hi : lo, &cnt, lane);
                 if (lane == 0 && cnt >= static_cast<uint32_t>(kTopK) && nb > lo) {
                   const uint32_t prev = atomicMax(s_cut, nb);
                   *reinterpret_cast<volatile float*>(s_cutf) = bin_floor_score(max(prev, nb));
@@ -1301,8 +1309,49 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
     warp_sort_desc<R>(v, lane);
     if (t < sd.T && !*s_abort) write_output<R>(p, sd.q_row0 + t, v, lane);
   };
+  auto shared_cut_role = [&]() {
+    // ================= one-query split plans: a cut shared by the sequence's splits. Each split
+    // publishes a bin its k-th best key reaches (k = ceil(512 / splits); the counts only grow,
+    // so a bin read from them stays valid); once every split has published, the lowest of
+    // those bins is reached by at least 512 keys of the sequence, so the sequence's 512th best
+    // lies at or above it, and this split's running cut is raised to it: fewer keys are listed
+    // and published. Counts at or above the final cut stay exact, which the merge relies on.
+    const int ns = sd.n_splits;
+    const uint32_t k = static_cast<uint32_t>((kTopK + ns - 1) / ns);
+    uint32_t* pub = p.counters + kCounterWords * (sd.ticket0 + qb) + 1;  // [ns]: bin + 1, 0 = none
+    uint32_t published = 0u;
+    const uint64_t t_start = globaltimer_ns();
+    // (bounded like every wait here: it also ends after the kernel's wait limit)
+    while (!*s_stream_done && !*s_abort && globaltimer_ns() - t_start < p.wait_ns) {
+      __nanosleep(1000);
+      uint32_t lo = 0u, hi = 0u, cnt;
+      if (lane == 0) {
+        lo = *reinterpret_cast<volatile uint32_t*>(s_cut);
+        hi = *reinterpret_cast<volatile uint32_t*>(s_maxbin);
+      }
+      lo = __shfl_sync(0xffffffffu, lo, 0);
+      hi = __shfl_sync(0xffffffffu, hi, 0);
+      const uint32_t b = warp_find_cut_grouped(k, s_bins, s_grp, lo, hi >= lo ? hi : lo, &cnt, lane);
+      if (lane == 0 && cnt >= k && b + 1u > published) {
+        published = b + 1u;
+        *reinterpret_cast<volatile uint32_t*>(pub + split) = published;
+      }
+      uint32_t low = 0xFFFFFFFFu;
+      for (int i = lane; i < ns; i += 32)
+        low = min(low, *reinterpret_cast<volatile uint32_t*>(pub + i));
+      low = __reduce_min_sync(0xffffffffu, low);
+      if (lane == 0 && low > 0u && low - 1u > *reinterpret_cast<volatile uint32_t*>(s_cut)) {
+        const uint32_t prev = atomicMax(s_cut, low - 1u);
+        *reinterpret_cast<volatile float*>(s_cutf) = bin_floor_score(max(prev, low - 1u));
+      }
+    }
+  };
   auto sel_role = [&]() {
     // ================= selectors
+    if (buffered) {
+      if (sd.n_splits > 1 && warp == C::kSelWarp0) shared_cut_role();
+      return;
+    }
     const int sidx = warp - C::kSelWarp0;
     const int q = sidx / C::kSelPerQuery;
     const int g0 = (sidx % C::kSelPerQuery) * C::kGroupsPerSel;  // first 32-key group it filters
@@ -1395,7 +1444,7 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
   if (!DENSE && sd.n_splits > 1) {
     // Split plans: every CTA of a query block takes a ticket after publishing its lists; the
     // CTA that takes the last ticket merges them (nothing ever waits on another CTA).
-    uint32_t* ticket = p.counters + sd.ticket0 + qb;
+    uint32_t* ticket = p.counters + kCounterWords * (sd.ticket0 + qb);
     __syncthreads();  // every thread's list writes (and proxy fence) precede the ticket
     if (threadIdx.x == 0) {
       __threadfence();
@@ -1412,7 +1461,9 @@ __global__ void __launch_bounds__(KCfg<DT, NQ, DENSE>::kThreads, 1)
           merge_split_lists<C>(p, sd, t0, reinterpret_cast<uint64_t*>(sK), sHist, s_scratch,
                                warp, lane);
       }
-      if (threadIdx.x == 0) *ticket = 0u;  // ready for the next call
+      // ready for the next call: the ticket and (one-query splits) the published bins
+      for (int i = threadIdx.x; i < (C::kHistSel ? 1 + sd.n_splits : 1); i += C::kThreads)
+        ticket[i] = 0u;
     }
   }
 }
