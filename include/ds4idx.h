@@ -179,13 +179,14 @@ uint64_t ds4idx_kernels_launched(void);
  * library holds that array until the process exits.
  *  - dtype is a ds4idx_dtype. All other arguments, layouts and rules are those of
  *    ds4idx_score_topk_batched, with 1 <= B <= 64, 0 <= T, 1 <= S < 2^31 and topk = 512.
- *  - Limit: the array holds 2^21 list words (16 MiB) and the split counters (merge ticket and
- *    the splits' published bins) of 4096 query blocks. Short sequences (decode, small chunks)
- *    split their key range over several CTAs, and each split publishes a list of 512 words per
- *    query (1152 per one-query sequence). Here the split count steps down from the one ds4idx_score_topk_batched would use until the lists fit
- *    (B * T * splits * 512 <= 2^21); one split needs no list, so every valid call runs, only
- *    with fewer CTAs where the handle path would split further. Outputs are the same as the
- *    handle path's. DS4IDX_ERR_SCRATCH_LIMIT is returned only if a plan still did not fit.
+ *  - Limit: the array holds 2^21 list words (16 MiB) and the split counters (merge ticket and the
+ *    splits' published bins) of 4096 query blocks. Short sequences (decode, small chunks) split
+ *    their key range over several CTAs, and each split publishes a list of 512 words per query
+ *    (1152 per one-query sequence). Here the split count steps down from the one
+ *    ds4idx_score_topk_batched would use until the lists fit (B * T * splits * 512 <= 2^21); one
+ *    split needs no list, so every valid call runs, only with fewer CTAs where the handle path
+ *    would split further. Outputs are the same as the handle path's. DS4IDX_ERR_SCRATCH_LIMIT is
+ *    returned only if a plan still did not fit.
  *  - Set-up: the first call on each device looks up the array's device address and sets kernel
  *    attributes, with that device current. Make that first call before any stream capture.
  *  - Argument errors return INVALID_ARG before anything is enqueued or the array is touched.
