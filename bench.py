@@ -202,7 +202,8 @@ def cpu_baseline(probs, budget_s=10.0):
         dt = time.perf_counter() - t0
         return {"value": len(probs) / dt, "unit": UNIT, "cores": orc.num_threads(),
                 "kind": "oracle",
-                "sample": f"all {len(probs)} decode queries ({probs[0].S} keys each), {dt:.1f} s"}
+                "sample": f"all {len(probs)} decode queries ({probs[0].S} keys each), {dt:.1f} s "
+                          f"(the oracle scores a row on one thread; its key decode uses all)"}
     prob = probs[0]
     q, k = prob.codes()
     ks = None if prob.kscale is None else prob.kscale.numpy()
@@ -224,29 +225,65 @@ def cpu_baseline(probs, budget_s=10.0):
                       f"{prob.name} (full causal rows, fp64 scores + full sort), {dt:.1f} s"}
 
 
+REF_STEP_S = 1.0  # oracle seconds per reference-arm step
+
+
+def even_rows(T, n, phase):
+    """n query rows spread evenly over [0, T) and shifted by `phase` in [0, 1): a sample with the
+    workload's mix of causal row lengths, different for each phase."""
+    n = max(1, min(int(n), T))
+    return np.unique(np.minimum(((np.arange(n) + phase) * (T / n)).astype(np.int64), T - 1))
+
+
 def run_reference(args, rank, world):
-    """Reference arm: the fp64 CPU oracle, timed on this host's cores (rank 0 only)."""
+    """Reference arm: the fp64 CPU oracle, timed on this host's cores (rank 0 only). Each step is
+    the same kind of sample `cpu_baseline` times: one decode query (the job's sequences in turn),
+    or about REF_STEP_S seconds of query rows spread evenly over the sequence (a new phase each
+    step)."""
     if rank != 0:
         return
     probs, _ = load_job(args.workload)
     prob = probs[0]
     from oracle import oracle as orc
-    q, k = prob.codes()
-    ks = None if prob.kscale is None else prob.kscale.numpy()
-    w = prob.w.numpy()
     threads = orc.num_threads()
     rng = np.random.default_rng(0)
-    per_step = max(threads, 16)
+    if len(probs) > 1:  # independent decode sequences: one query per step, in turn
+        prepared = [(p, *p.codes()) for p in probs]
+        turn = [0]
+
+        def one_step():
+            p, q, k = prepared[turn[0] % len(prepared)]
+            turn[0] += 1
+            orc.topk(p.dtype, q, p.w.numpy(), k, p.kscale.numpy(), p.pos_offset, p.topk)
+            return 1
+        sample = (f"one decode query ({prob.S} keys) per step, the job's {len(probs)} "
+                  f"sequences in turn (the oracle scores a row on one thread; its key decode "
+                  f"uses all)")
+    else:
+        q, k = prob.codes()
+        ks = None if prob.kscale is None else prob.kscale.numpy()
+        w = prob.w.numpy()
+        n_cal = min(prob.T, 4 * threads)
+        t0 = time.perf_counter()
+        orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, even_rows(prob.T, n_cal, 0.5))
+        dt = max(time.perf_counter() - t0, 1e-3)
+        per_step = int(min(prob.T, max(n_cal, n_cal * REF_STEP_S / dt)))
+
+        def one_step():
+            rows = even_rows(prob.T, per_step, rng.random())
+            orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, rows)
+            return len(rows)
+        sample = (f"{per_step} query rows per step spread evenly over t in [0, {prob.T}) with a "
+                  f"random phase, of {prob.name} (full causal rows, fp64 scores + full sort)")
     times = []
     done = 0
     for step in range(args.warmup + args.steps):
-        rows = np.sort(rng.integers(0, prob.T, size=per_step))
         t0 = time.perf_counter()
-        orc.topk(prob.dtype, q, w, k, ks, prob.pos_offset, prob.topk, rows)
+        n = one_step()
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             times.append(dt)
-            done += len(rows)
+            done += n
     total = sum(times)
     value = done / total
     out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
@@ -257,8 +294,7 @@ def run_reference(args, rank, world):
                       "H_I": inputs.H_I, "d_I": inputs.D_I, "topk": prob.topk,
                       "pos_offset": prob.pos_offset, "seed": prob.meta.get("seed")},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                            "sample": f"{per_step} random query rows per step of {prob.name} "
-                                      f"(full causal rows, fp64 scores + full sort)"},
+                            "sample": sample},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)

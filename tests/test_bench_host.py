@@ -28,3 +28,17 @@ def test_all_bytes_counts_inputs_and_outputs_once():
     # 64k bf16 prefill: q 1 GiB + w 16 MiB + keys 16 MiB + outputs 256 MiB
     assert bench.all_bytes(_P(65536, 65536, 0, inputs.BF16)) == pytest.approx(
         2**30 + 2**24 + 2**24 + 2**28)
+
+
+@pytest.mark.parametrize("T,n", [(65536, 104), (65536, 1), (7, 7), (7, 20), (1, 16)])
+def test_reference_rows_are_spread_evenly(T, n):
+    import numpy as np
+    for phase in (0.0, 0.37, 0.999):
+        rows = bench.even_rows(T, n, phase)
+        m = min(n, T)
+        assert len(rows) == m and rows.min() >= 0 and rows.max() < T
+        assert np.all(np.diff(rows) > 0)
+        # row i is the floor of a point of the i-th of m equal strata of [0, T): the causal row
+        # lengths' mix
+        i = np.arange(m)
+        assert np.all(rows >= i * T // m) and np.all(rows * m < (i + 1) * T)
